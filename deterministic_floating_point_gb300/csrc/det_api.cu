@@ -1,0 +1,69 @@
+// Status reporting and measurement hooks for the C ABI.
+#include "det_common.cuh"
+#include "../../include/det_profile.h"
+
+namespace {
+struct Profile {
+  cudaEvent_t* events = nullptr;
+  int capacity = 0;
+  int count = 0;
+  int open = 0;
+  const char* names[4096];
+};
+Profile g_prof;
+unsigned long long g_launches = 0;
+}  // namespace
+
+namespace det {
+void launch_begin(const char* name, cudaStream_t s) {
+  ++g_launches;
+  if (g_prof.events && g_prof.count < g_prof.capacity && g_prof.count < 4096) {
+    cudaEventRecord(g_prof.events[2 * g_prof.count], s);
+    g_prof.names[g_prof.count] = name;
+    g_prof.open = 1;
+  }
+}
+void launch_end(cudaStream_t s) {
+  if (g_prof.open) {
+    cudaEventRecord(g_prof.events[2 * g_prof.count + 1], s);
+    ++g_prof.count;
+    g_prof.open = 0;
+  }
+}
+}  // namespace det
+
+extern "C" int det_profile_set_events(void* const* events, int capacity) {
+  g_prof.events = (events && capacity > 0) ? (cudaEvent_t*)events : nullptr;
+  g_prof.capacity = g_prof.events ? capacity : 0;
+  g_prof.count = 0;
+  g_prof.open = 0;
+  return 0;
+}
+extern "C" int det_profile_event_count(void) { return g_prof.count; }
+extern "C" const char* det_profile_event_name(int i) {
+  return (i >= 0 && i < g_prof.count) ? g_prof.names[i] : nullptr;
+}
+extern "C" unsigned long long det_launch_count(void) { return g_launches; }
+
+extern "C" int det_read_status(const void* workspace, void* stream, int* device_status) {
+  if (!workspace || !device_status) return DET_ERR_INVALID_ARG;
+  cudaStream_t s = det::as_stream(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DET_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return DET_ERR_CUDA;
+  *device_status = (int)v;
+  return DET_OK;
+}
+
+extern "C" const char* det_status_string(int status) {
+  switch (status) {
+    case DET_OK: return "ok";
+    case DET_ERR_INVALID_ARG: return "invalid argument";
+    case DET_ERR_DTYPE: return "unsupported dtype (use DET_F32 or DET_F64)";
+    case DET_ERR_TOO_LARGE: return "size beyond the documented limit";
+    case DET_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
+    case DET_ERR_LOOKBACK_TIMEOUT: return "device: a look-back wait gave up";
+    case DET_ERR_CUDA: return "CUDA call or launch failed";
+    default: return "unknown status";
+  }
+}

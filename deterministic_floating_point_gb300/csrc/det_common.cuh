@@ -1,0 +1,144 @@
+// Shared device helpers for the deterministic reductions (sm_103a).
+//
+// Only IEEE round-to-nearest additions of the data type touch values.  The
+// build uses no fast-math and leaves flush-to-zero off; there are no
+// multiplies on any value path, so FMA contraction cannot arise.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/det.h"
+
+namespace det {
+
+constexpr int kWarp = 32;
+
+// Workspace header: the first 256 bytes of every workspace.
+struct WsHeader {
+  unsigned int status;     // DET_OK or a device-detected error code
+  unsigned int ticket;     // per-call integer ticket (order-safe: integer adds)
+  unsigned int ticket2;
+  unsigned int pad_[61];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+constexpr size_t kHeaderBytes = 256;
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// "absent" term: x + (-0.0) == x for every x under round to nearest.
+template <typename T> __device__ __forceinline__ T absent() { return T(-0.0); }
+
+// ---------------------------------------------------------------------------
+// 256-bit loads (one 32-byte sector per lane).  The pointer must be 32-byte
+// aligned.  Read-only path; the data are not written by the same kernel.
+__device__ __forceinline__ void ld_nc_256(const float* p, float (&v)[8]) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
+                 "=f"(v[6]), "=f"(v[7])
+               : "l"(p));
+}
+__device__ __forceinline__ void ld_nc_256(const double* p, double (&v)[4]) {
+  asm volatile("ld.global.nc.L1::no_allocate.v4.f64 {%0,%1,%2,%3}, [%4];"
+               : "=d"(v[0]), "=d"(v[1]), "=d"(v[2]), "=d"(v[3])
+               : "l"(p));
+}
+
+// Plain (coherent) 256-bit load, for data another block of this grid may have
+// written earlier in the same launch.
+__device__ __forceinline__ void ld_256(const float* p, float (&v)[8]) {
+  asm volatile("ld.global.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
+                 "=f"(v[6]), "=f"(v[7])
+               : "l"(p)
+               : "memory");
+}
+__device__ __forceinline__ void ld_256(const double* p, double (&v)[4]) {
+  asm volatile("ld.global.v4.f64 {%0,%1,%2,%3}, [%4];"
+               : "=d"(v[0]), "=d"(v[1]), "=d"(v[2]), "=d"(v[3])
+               : "l"(p)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_256(float* p, const float (&v)[8]) {
+  asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(v[0]),
+               "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+               : "memory");
+}
+__device__ __forceinline__ void st_256(double* p, const double (&v)[4]) {
+  asm volatile("st.global.v4.f64 [%0], {%1,%2,%3,%4};" ::"l"(p), "d"(v[0]), "d"(v[1]),
+               "d"(v[2]), "d"(v[3])
+               : "memory");
+}
+
+template <typename T> struct Vec256;
+template <> struct Vec256<float> { static constexpr int N = 8; };
+template <> struct Vec256<double> { static constexpr int N = 4; };
+
+// ---------------------------------------------------------------------------
+// Canonical pairwise tree over N (a power of two) values held in registers:
+// level by level, v[i] = v[i] + v[i + s] for i a multiple of 2s.
+template <typename T, int N>
+__device__ __forceinline__ T thread_pt(T (&v)[N]) {
+  static_assert((N & (N - 1)) == 0, "N must be a power of two");
+#pragma unroll
+  for (int s = 1; s < N; s <<= 1) {
+#pragma unroll
+    for (int i = 0; i < N; i += 2 * s) v[i] = v[i] + v[i + s];
+  }
+  return v[0];
+}
+
+// Five tree levels across the 32 lanes of a warp: at level s lane l adds the
+// value of lane l ^ s.  For the lower lane of each pair this is the pair
+// (2j, 2j+1) of the tree, and IEEE addition is commutative, so every lane ends
+// with the bits of PT over lanes 0..31.
+template <typename T>
+__device__ __forceinline__ T warp_pt(T v) {
+#pragma unroll
+  for (int s = 1; s < kWarp; s <<= 1) v = v + __shfl_xor_sync(0xffffffffu, v, s);
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Memory-model helpers for flags and published values.
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned int* p, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void ld_acquire_v2u64(const unsigned long long* p, unsigned long long& a,
+                                                 unsigned long long& b) {
+  asm volatile("ld.acquire.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
+// Record a device-detected error in the status word (first error wins).
+__device__ __forceinline__ void set_status(unsigned int* status, unsigned int code) {
+  atomicCAS(status, 0u, code);
+}
+
+// Host-side helpers -----------------------------------------------------------
+inline bool valid_block_threads(int bt) {
+  return bt == 0 || bt == 128 || bt == 256 || bt == 512 || bt == 1024;
+}
+inline int elem_size(int dtype) { return dtype == DET_F32 ? 4 : 8; }
+inline bool valid_dtype(int dtype) { return dtype == DET_F32 || dtype == DET_F64; }
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Launch bookkeeping for the measurement hooks of det_profile.h.  Every
+// kernel launch of the library goes through launch_begin / launch_end.
+void launch_begin(const char* name, cudaStream_t s);
+void launch_end(cudaStream_t s);
+
+}  // namespace det

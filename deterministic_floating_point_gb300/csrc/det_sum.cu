@@ -1,0 +1,203 @@
+// det_sum: the canonical pairwise tree over element index, in one launch.
+//
+// Day 68 "Floating point and reproducibility" ("Contracts from tolerance to
+// fixed bits", items 1-2; "Fix the order of every addition") replaces the
+// scheduler-ordered atomic tail with a fixed tree, but its tree is a function
+// of the grid.  Here the tree is PT over element index: node (level k, j)
+// covers elements [j 2^k, (j+1) 2^k).  Any split of the input into aligned
+// power-of-two tiles, followed by PT over the tile results, gives exactly
+// those nodes, so neither the block size nor the grid enters the bits.
+//
+// Layout of the work:
+//   lane       128 contiguous bytes (32 f32 / 16 f64) = 4 x 256-bit loads,
+//              reduced in registers by PT                 -> level 5 / 4 node
+//   warp-block 32 lanes = 4 KB, five xor-shuffle levels      -> level 10 / 9
+//   tile       2^tb warp-blocks per CTA (host-chosen power of two), nodes
+//              staged in shared memory and reduced by PT
+//   final      the last CTA to finish (integer ticket) reduces the tile
+//              partials by PT and writes the scalar.
+#include "det_common.cuh"
+
+namespace det {
+namespace {
+
+template <typename T> struct SumGeom {
+  static constexpr int LE = 128 / sizeof(T);   // elements per lane
+  static constexpr int WB = kWarp * LE;        // elements per warp-block
+  static constexpr int V = Vec256<T>::N;       // elements per 256-bit load
+};
+
+// PT over p[0..L) by a whole CTA; the result is returned to thread 0.
+// Thread t reduces the aligned group [t g, (t+1) g) with g = max(1, P / T)
+// (P = next power of two >= L) by an in-thread binary counter; the thread
+// nodes are then reduced by warp_pt and a final PT over the warp nodes.
+template <typename T>
+__device__ T cta_pt_global(const T* p, long long L, T* smem_warp) {
+  const int nthreads = blockDim.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
+  long long P = 1;
+  while (P < L) P <<= 1;
+  long long g = P / nthreads;
+  if (g < 1) g = 1;
+  T node = absent<T>();
+  {
+    long long lo = (long long)tid * g;
+    T stack[40];
+    long long cnt = 0;
+    for (long long i = 0; i < g; ++i) {
+      long long idx = lo + i;
+      T v = (idx < L) ? __ldcg(p + idx) : absent<T>();
+      int lvl = 0;
+      long long c = cnt;
+      while (c & 1) {
+        v = stack[lvl] + v;
+        c >>= 1;
+        ++lvl;
+      }
+      stack[lvl] = v;
+      ++cnt;
+    }
+    // g is a power of two, so the counter ends with one full node
+    int top = 0;
+    while ((1LL << top) < g) ++top;
+    node = stack[top];
+  }
+  node = warp_pt(node);
+  if (lane == 0) smem_warp[warp] = node;
+  __syncthreads();
+  T r = absent<T>();
+  if (warp == 0) {
+    T v = lane < nwarps ? smem_warp[lane] : absent<T>();
+    r = warp_pt(v);
+  }
+  __syncthreads();
+  return r;
+}
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(1024)
+sum_kernel(const T* __restrict__ x, long long n, int tb_log2, long long ntiles, T* __restrict__ partials,
+           unsigned int* __restrict__ ticket, T* __restrict__ out) {
+  using G = SumGeom<T>;
+  __shared__ T nodes[1024];
+  __shared__ T warp_nodes[32];
+  __shared__ int is_last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int TB = 1 << tb_log2;
+  const long long tile_base = (long long)blockIdx.x * TB * G::WB;
+
+  for (int b = warp; b < TB; b += nwarps) {
+    const long long base = tile_base + (long long)b * G::WB + (long long)lane * G::LE;
+    T v[G::LE];
+    if (VEC && base + G::LE <= n) {
+#pragma unroll
+      for (int q = 0; q < G::LE / G::V; ++q) {
+        T w[G::V];
+        ld_nc_256(x + base + q * G::V, w);
+#pragma unroll
+        for (int e = 0; e < G::V; ++e) v[q * G::V + e] = w[e];
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < G::LE; ++e) v[e] = (base + e < n) ? x[base + e] : absent<T>();
+    }
+    T node = warp_pt(thread_pt(v));
+    if (lane == 0) nodes[b] = node;
+  }
+  __syncthreads();
+
+  // PT over the TB warp-block nodes of this tile, by warp 0.
+  if (warp == 0) {
+    const int per = TB > 32 ? TB / 32 : 1;   // aligned group per lane
+    T acc[32];
+    T node;
+    if (per == 1) {
+      node = lane < TB ? nodes[lane] : absent<T>();
+    } else {
+      // per is a power of two <= 32: level-by-level PT over the lane's group
+      for (int i = 0; i < per; ++i) acc[i] = nodes[lane * per + i];
+      for (int s = 1; s < per; s <<= 1)
+        for (int i = 0; i < per; i += 2 * s) acc[i] = acc[i] + acc[i + s];
+      node = acc[0];
+    }
+    node = warp_pt(node);
+    if (lane == 0) {
+      partials[blockIdx.x] = node;
+      __threadfence();
+      unsigned int t = atomicAdd(ticket, 1u);
+      is_last = (t == (unsigned int)(ntiles - 1));
+    }
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  // Partials were written by other CTAs: read them through L2 (volatile).
+  T r = cta_pt_global<T>((const T*)partials, ntiles, warp_nodes);
+  if (threadIdx.x == 0) *out = r;
+}
+
+}  // namespace
+
+// Tile size: a power of two number of 4 KB warp-blocks chosen from n only
+// (the bits do not depend on it; only the grid does).
+static int sum_tile_log2(long long nblocks) {
+  long long want = nblocks / 600;
+  int t = 0;
+  while (t < 10 && (2LL << t) <= want) ++t;
+  return t;
+}
+
+template <typename T>
+static long long sum_ntiles(long long n, int* tb_log2) {
+  long long nblocks = (n + SumGeom<T>::WB - 1) / SumGeom<T>::WB;
+  int t = sum_tile_log2(nblocks);
+  if (tb_log2) *tb_log2 = t;
+  return (nblocks + (1LL << t) - 1) >> t;
+}
+
+}  // namespace det
+
+using namespace det;
+
+extern "C" size_t det_sum_workspace_bytes(int64_t n, int dtype) {
+  if (n < 0 || !valid_dtype(dtype)) return 0;
+  long long nt = dtype == DET_F32 ? sum_ntiles<float>(n, nullptr) : sum_ntiles<double>(n, nullptr);
+  return kHeaderBytes + align_up((size_t)nt * elem_size(dtype), 256);
+}
+
+template <typename T>
+static int det_sum_impl(const T* x, long long n, T* out, void* ws, size_t ws_bytes, int bt,
+                        cudaStream_t s) {
+  int tb;
+  long long nt = sum_ntiles<T>(n, &tb);
+  if (ws_bytes < det_sum_workspace_bytes(n, sizeof(T) == 4 ? DET_F32 : DET_F64)) return DET_ERR_WORKSPACE;
+  WsHeader* h = reinterpret_cast<WsHeader*>(ws);
+  if (cudaMemsetAsync(h, 0, kHeaderBytes, s) != cudaSuccess) return DET_ERR_CUDA;
+  if (n == 0) {
+    if (cudaMemsetAsync(out, 0, sizeof(T), s) != cudaSuccess) return DET_ERR_CUDA;
+    return DET_OK;
+  }
+  T* partials = reinterpret_cast<T*>(reinterpret_cast<char*>(ws) + kHeaderBytes);
+  const int threads = bt ? bt : (tb >= 3 ? 256 : 32 << tb);
+  const bool vec = (reinterpret_cast<uintptr_t>(x) % 32) == 0;
+  launch_begin("det_sum", s);
+  if (vec)
+    sum_kernel<T, true><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out);
+  else
+    sum_kernel<T, false><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out);
+  launch_end(s);
+  return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
+}
+
+extern "C" int det_sum(const void* x, int64_t n, int dtype, void* out, void* workspace,
+                       size_t workspace_bytes, int block_threads, void* stream) {
+  if (!valid_dtype(dtype)) return DET_ERR_DTYPE;
+  if (n < 0 || !out || !workspace || (n > 0 && !x) || !valid_block_threads(block_threads))
+    return DET_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256) return DET_ERR_WORKSPACE;
+  if (dtype == DET_F32)
+    return det_sum_impl<float>((const float*)x, n, (float*)out, workspace, workspace_bytes,
+                               block_threads, as_stream(stream));
+  return det_sum_impl<double>((const double*)x, n, (double*)out, workspace, workspace_bytes,
+                              block_threads, as_stream(stream));
+}

@@ -1,0 +1,265 @@
+"""Thin Python binding over the C ABI of ``libdet.so`` (see ``include/det.h``).
+
+Argument marshalling only: tensors become raw device pointers and sizes, the
+current torch stream becomes the ``stream`` argument, and a workspace of the
+size the library asks for is taken from torch's allocator when the caller
+does not pass one.  Every step of every operation runs in the library's CUDA
+kernels; there is no fallback.  If ``libdet.so`` is missing or cannot be
+loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdet.so")
+
+F32, F64 = 0, 1
+OK = 0
+SCAN_INCLUSIVE, SCAN_EXCLUSIVE, SCAN_REVERSE = 0, 1, 2
+SCAN_LANE_ELEMS = {torch.float32: 32, torch.float64: 16}
+SCAN_CHUNK = {torch.float32: 32768, torch.float64: 16384}
+
+_lock = threading.Lock()
+_lib = None
+
+_i64, _sz, _vp, _int = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int
+_SIGNATURES = {
+    "det_sum_workspace_bytes": (_sz, [_i64, _int]),
+    "det_sum": (_int, [_vp, _i64, _int, _vp, _vp, _sz, _int, _vp]),
+    "det_scatter_add_workspace_bytes": (_sz, [_i64, _i64, _int]),
+    "det_scatter_add": (_int, [_vp, _i64, _vp, _vp, _i64, _int, _vp, _vp, _vp, _sz, _int, _vp]),
+    "det_scatter_add_rows_workspace_bytes": (_sz, [_i64, _i64, _i64, _int]),
+    "det_scatter_add_rows": (_int, [_vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _int, _vp, _sz, _int, _vp]),
+    "det_scan_workspace_bytes": (_sz, [_i64, _int]),
+    "det_scan": (_int, [_vp, _vp, _i64, _int, _int, _vp, _vp, _sz, _int, _vp]),
+    "det_segmented_scan_workspace_bytes": (_sz, [_i64, _i64, _int]),
+    "det_segmented_scan": (_int, [_vp, _vp, _i64, _vp, _i64, _int, _int, _vp, _sz, _int, _vp]),
+    "det_read_status": (_int, [_vp, _vp, ctypes.POINTER(_int)]),
+    "det_status_string": (ctypes.c_char_p, [_int]),
+    "det_profile_set_events": (_int, [_vp, _int]),
+    "det_profile_event_count": (_int, []),
+    "det_profile_event_name": (ctypes.c_char_p, [_int]),
+    "det_launch_count": (ctypes.c_ulonglong, []),
+}
+
+
+class DetError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} (code {code})")
+
+
+def lib():
+    """The loaded ``libdet.so``; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it first "
+                                   "(python -c 'import __graft_entry__ as g; g.build()')")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(handle, name, None)
+                if fn is None:
+                    continue
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+    return _lib
+
+
+def exported_symbols():
+    h = lib()
+    return {name for name in _SIGNATURES if getattr(h, name, None) is not None}
+
+
+def status_string(code: int) -> str:
+    try:
+        return lib().det_status_string(int(code)).decode()
+    except Exception:  # pragma: no cover - only when the library is absent
+        return "unknown"
+
+
+def _code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.float64:
+        return F64
+    raise TypeError(f"det supports float32 and float64 tensors, got {t.dtype}")
+
+
+def _dev(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """A device byte buffer with a 256-byte aligned start of at least nbytes."""
+    buf = torch.empty(int(nbytes) + 256, dtype=torch.uint8, device=device)
+    off = (-buf.data_ptr()) % 256
+    return buf[off:off + int(nbytes)]
+
+
+def _ws(ws, nbytes, device):
+    if ws is None:
+        ws = workspace(nbytes, device)
+    if ws.numel() < nbytes:
+        raise DetError(4, "workspace")
+    return ws
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise DetError(rc, what)
+
+
+def read_status(ws: torch.Tensor, stream=None) -> int:
+    st = _int(0)
+    _check(lib().det_read_status(_ptr(ws), _stream(stream), ctypes.byref(st)), "det_read_status")
+    return int(st.value)
+
+
+# ---------------------------------------------------------------------------
+
+
+def det_sum(x: torch.Tensor, out: torch.Tensor | None = None, *, block_threads: int = 0,
+            workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[0] = pairwise tree sum of x (see det.h)."""
+    _dev(x, "x")
+    code = _code(x)
+    if out is None:
+        out = torch.empty(1, dtype=x.dtype, device=x.device)
+    n = x.numel()
+    nbytes = lib().det_sum_workspace_bytes(n, code)
+    ws = _ws(workspace, nbytes, x.device)
+    _check(lib().det_sum(_ptr(x), n, code, _ptr(out), _ptr(ws), ws.numel(), block_threads,
+                         _stream(stream)), "det_sum")
+    return out
+
+
+def det_scatter_add(out: torch.Tensor, bins: torch.Tensor, values: torch.Tensor, *,
+                    perm_out: torch.Tensor | None = None, seg_offsets_out: torch.Tensor | None = None,
+                    block_threads: int = 0, workspace: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """out[bins[i]] += values[i], in a fixed order (see det.h); returns out."""
+    _dev(out, "out"), _dev(bins, "bins"), _dev(values, "values")
+    code = _code(values)
+    if out.dtype != values.dtype or bins.dtype != torch.int32:
+        raise TypeError("out must match values' dtype and bins must be int32")
+    n, m = values.numel(), out.numel()
+    if bins.numel() != n:
+        raise ValueError("bins and values differ in length")
+    nbytes = lib().det_scatter_add_workspace_bytes(n, m, code)
+    ws = _ws(workspace, nbytes, values.device)
+    _check(lib().det_scatter_add(_ptr(out), m, _ptr(bins), _ptr(values), n, code, _ptr(perm_out),
+                                 _ptr(seg_offsets_out), _ptr(ws), ws.numel(), block_threads,
+                                 _stream(stream)), "det_scatter_add")
+    return out
+
+
+def det_scatter_add_rows(dst: torch.Tensor, idx: torch.Tensor, src: torch.Tensor, *, row_offset: int = 0,
+                         prev_out: torch.Tensor | None = None, block_threads: int = 0,
+                         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """dst[idx[s] + row_offset] += src[s] row by row, in a fixed order; returns dst."""
+    _dev(dst, "dst"), _dev(idx, "idx"), _dev(src, "src")
+    code = _code(src)
+    if dst.dim() != 2 or src.dim() != 2 or dst.shape[1] != src.shape[1] or dst.dtype != src.dtype:
+        raise ValueError("dst and src must be 2-D of one dtype with equal row length")
+    if idx.dtype != torch.int32 or idx.numel() != src.shape[0]:
+        raise ValueError("idx must be int32 with one entry per source row")
+    R, W = dst.shape
+    M = src.shape[0]
+    nbytes = lib().det_scatter_add_rows_workspace_bytes(M, R, W, code)
+    ws = _ws(workspace, nbytes, src.device)
+    _check(lib().det_scatter_add_rows(_ptr(dst), R, W, _ptr(idx), int(row_offset), _ptr(src), M,
+                                      _ptr(prev_out), code, _ptr(ws), ws.numel(), block_threads,
+                                      _stream(stream)), "det_scatter_add_rows")
+    return dst
+
+
+def det_scan(x: torch.Tensor, y: torch.Tensor | None = None, *, flags: int = SCAN_INCLUSIVE,
+             total_out: torch.Tensor | None = None, block_threads: int = 0,
+             workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Anchored look-back prefix sum (see det.h); y may be x; returns y."""
+    _dev(x, "x")
+    code = _code(x)
+    if y is None:
+        y = torch.empty_like(x)
+    n = x.numel()
+    nbytes = lib().det_scan_workspace_bytes(n, code)
+    ws = _ws(workspace, nbytes, x.device)
+    _check(lib().det_scan(_ptr(x), _ptr(y), n, code, int(flags), _ptr(total_out), _ptr(ws), ws.numel(),
+                          block_threads, _stream(stream)), "det_scan")
+    return y
+
+
+def det_segmented_scan(x: torch.Tensor, seg_offsets: torch.Tensor, y: torch.Tensor | None = None, *,
+                       flags: int = SCAN_INCLUSIVE, block_threads: int = 0,
+                       workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Segmented anchored look-back prefix sum over int64 CSR offsets."""
+    _dev(x, "x"), _dev(seg_offsets, "seg_offsets")
+    code = _code(x)
+    if seg_offsets.dtype != torch.int64:
+        raise TypeError("seg_offsets must be int64")
+    if y is None:
+        y = torch.empty_like(x)
+    n, S = x.numel(), seg_offsets.numel() - 1
+    nbytes = lib().det_segmented_scan_workspace_bytes(n, S, code)
+    ws = _ws(workspace, nbytes, x.device)
+    _check(lib().det_segmented_scan(_ptr(x), _ptr(y), n, _ptr(seg_offsets), S, code, int(flags), _ptr(ws),
+                                    ws.numel(), block_threads, _stream(stream)), "det_segmented_scan")
+    return y
+
+
+# ---------------------------------------------------------------------------
+# measurement hooks (include/det_profile.h)
+
+
+class KernelTimer:
+    """Records a CUDA event pair around each kernel the library launches
+    while active; ``kernels()`` returns [(name, ms), ...] in launch order."""
+
+    def __init__(self, capacity: int = 256):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * capacity)]
+        for e in self.events:
+            e.record()  # materialise the underlying cudaEvent_t
+        torch.cuda.synchronize()
+        self._arr = (ctypes.c_void_p * len(self.events))(*[e.cuda_event for e in self.events])
+        self.capacity = capacity
+
+    def __enter__(self):
+        lib().det_profile_set_events(self._arr, self.capacity)
+        return self
+
+    def __exit__(self, *exc):
+        self._count = lib().det_profile_event_count()
+        self._names = [lib().det_profile_event_name(i).decode() for i in range(self._count)]
+        lib().det_profile_set_events(None, 0)
+        return False
+
+    def kernels(self):
+        torch.cuda.synchronize()
+        return [(self._names[i], self.events[2 * i].elapsed_time(self.events[2 * i + 1]))
+                for i in range(self._count)]
+
+
+def launch_count() -> int:
+    return int(lib().det_launch_count())

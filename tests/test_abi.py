@@ -1,0 +1,63 @@
+"""The C-ABI library loads and exports every function include/*.h declares;
+host-side argument checks answer without touching a GPU."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(det_[A-Za-z0-9_]+)\s*\(",
+                             text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from deterministic_floating_point_gb300 import _build, det
+    _build.build()
+    return det.lib()
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for fn in ("det_sum", "det_scatter_add", "det_scatter_add_rows", "det_scan", "det_segmented_scan",
+               "det_read_status", "det_status_string"):
+        assert fn in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in sorted(declared_functions()) if getattr(lib, n, None) is None]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    from deterministic_floating_point_gb300 import det
+    assert det.status_string(0) == "ok"
+    for code in range(1, 7):
+        assert det.status_string(code) != "unknown status"
+
+
+def test_host_argument_checks_need_no_gpu(lib):
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)            # never dereferenced: the checks fail first
+    assert lib.det_sum(fake, 10, 7, fake, fake, 1 << 20, 0, None) == 2          # dtype
+    assert lib.det_sum(None, 10, 0, fake, fake, 1 << 20, 0, None) == 1          # null x
+    assert lib.det_sum(fake, -1, 0, fake, fake, 1 << 20, 0, None) == 1          # n < 0
+    assert lib.det_sum(fake, 10, 0, fake, fake, 1 << 20, 96, None) == 1         # block size
+    assert lib.det_sum(fake, 10, 0, fake, vp((1 << 20) + 8), 1 << 20, 0, None) == 4  # misaligned ws
+
+
+def test_workspace_queries_are_host_only(lib):
+    assert lib.det_sum_workspace_bytes(0, 0) >= 256
+    assert lib.det_sum_workspace_bytes(1 << 28, 0) > lib.det_sum_workspace_bytes(1 << 20, 0)
+    assert lib.det_sum_workspace_bytes(-1, 0) == 0
