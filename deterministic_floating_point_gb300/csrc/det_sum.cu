@@ -16,6 +16,8 @@
 //              staged in shared memory and reduced by PT
 //   final      the last CTA to finish (integer ticket) reduces the tile
 //              partials by PT and writes the scalar.
+#include <mutex>
+
 #include "det_common.cuh"
 
 namespace det {
@@ -200,4 +202,68 @@ extern "C" int det_sum(const void* x, int64_t n, int dtype, void* out, void* wor
                                block_threads, as_stream(stream));
   return det_sum_impl<double>((const double*)x, n, (double*)out, workspace, workspace_bytes,
                               block_threads, as_stream(stream));
+}
+
+// ---------------------------------------------------------------------------
+// det_sum_noalloc: det_sum whose scratch (header + tile partials) lives in a
+// statically sized device array of this file instead of a workspace, for
+// callers that cannot allocate device memory.  The kernel is det_sum's.
+
+static __device__ __align__(256) unsigned char g_sum_noalloc_scratch[kHeaderBytes +
+                                                                     (size_t)DET_SUM_NOALLOC_MAX_PARTIALS *
+                                                                         sizeof(double)];
+
+namespace {
+constexpr int kMaxDevices = 128;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_scratch[kMaxDevices] = {};
+
+// Device address of the static array on the current device, looked up once
+// per device.  In host code g_sum_noalloc_scratch names a host-side stand-in,
+// never device memory, so only this address may be handed to a kernel.
+int noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DET_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_scratch[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_sum_noalloc_scratch) != cudaSuccess || !p) return DET_ERR_CUDA;
+    g_noalloc_scratch[dev] = p;
+  }
+  *out = g_noalloc_scratch[dev];
+  return DET_OK;
+}
+
+template <typename T>
+int det_sum_noalloc_impl(const T* x, long long n, T* out, int bt, cudaStream_t s) {
+  int tb;
+  const long long nt = sum_ntiles<T>(n, &tb);
+  if (nt > DET_SUM_NOALLOC_MAX_PARTIALS) return DET_ERR_TOO_LARGE;
+  void* scratch = nullptr;
+  const int rc = noalloc_scratch(&scratch);
+  if (rc != DET_OK) return rc;
+  WsHeader* h = reinterpret_cast<WsHeader*>(scratch);
+  // the ticket must start at zero; the partials are written before they are read
+  if (cudaMemsetAsync(h, 0, kHeaderBytes, s) != cudaSuccess) return DET_ERR_CUDA;
+  if (n == 0) return cudaMemsetAsync(out, 0, sizeof(T), s) == cudaSuccess ? DET_OK : DET_ERR_CUDA;
+  T* partials = reinterpret_cast<T*>(reinterpret_cast<char*>(scratch) + kHeaderBytes);
+  const int threads = bt ? bt : (tb >= 3 ? 256 : 32 << tb);
+  const bool vec = (reinterpret_cast<uintptr_t>(x) % 32) == 0;
+  launch_begin("det_sum_noalloc", s);
+  if (vec)
+    sum_kernel<T, true><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out);
+  else
+    sum_kernel<T, false><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out);
+  launch_end(s);
+  return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" int det_sum_noalloc(const void* x, int64_t n, int dtype, void* out, int block_threads,
+                               void* stream) {
+  if (!valid_dtype(dtype)) return DET_ERR_DTYPE;
+  if (n < 0 || !out || (n > 0 && !x) || !valid_block_threads(block_threads)) return DET_ERR_INVALID_ARG;
+  if (dtype == DET_F32)
+    return det_sum_noalloc_impl<float>((const float*)x, n, (float*)out, block_threads, as_stream(stream));
+  return det_sum_noalloc_impl<double>((const double*)x, n, (double*)out, block_threads, as_stream(stream));
 }

@@ -31,6 +31,7 @@ _i64, _sz, _vp, _int = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.
 _SIGNATURES = {
     "det_sum_workspace_bytes": (_sz, [_i64, _int]),
     "det_sum": (_int, [_vp, _i64, _int, _vp, _vp, _sz, _int, _vp]),
+    "det_sum_noalloc": (_int, [_vp, _i64, _int, _vp, _int, _vp]),
     "det_scatter_add_workspace_bytes": (_sz, [_i64, _i64, _int]),
     "det_scatter_add": (_int, [_vp, _i64, _vp, _vp, _i64, _int, _vp, _vp, _vp, _sz, _int, _vp]),
     "det_scatter_add_rows_workspace_bytes": (_sz, [_i64, _i64, _i64, _int]),

@@ -22,7 +22,8 @@
  *   that may run at the same time.
  * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *   stream).  Work is only enqueued: no call synchronizes, allocates or copies
- *   to the host, so every call can be captured in a CUDA graph.
+ *   to the host, so every call that takes a workspace can be captured in a
+ *   CUDA graph.
  * - `block_threads` selects the CUDA block size: 0 (the default) or one of
  *   128, 256, 512, 1024.  It changes the launch shape only, never the bits.
  * - Return value: DET_OK, or an error code for a bad argument found on the
@@ -82,6 +83,37 @@ extern "C" {
 size_t det_sum_workspace_bytes(int64_t n, int dtype);
 int det_sum(const void* x, int64_t n, int dtype, void* out,
             void* workspace, size_t workspace_bytes, int block_threads, void* stream);
+
+/* ------------------------------------------------------------------------
+ * det_sum_noalloc -- det_sum without any caller-provided or allocated
+ * scratch memory.  (The pages have no counterpart; this entry point exists
+ * for callers that cannot allocate.)
+ *
+ * Some callers cannot call cudaMalloc or hand the library a workspace: a
+ * plugin running inside another runtime that owns all device memory and
+ * exposes no allocator to it, or a loop that must not allocate after
+ * start-up because cudaMalloc can synchronize the device and has unbounded
+ * latency.  For them this call keeps its scratch (a 256-byte status/ticket
+ * header and up to DET_SUM_NOALLOC_MAX_PARTIALS tile partials) in one
+ * statically sized device array inside libdet.so, 256 + 16384 * 8 bytes,
+ * which every GPU that loads the library holds until the process exits.
+ * The caller still passes the input and the output; the result bits equal
+ * det_sum's.
+ *   x    device, n elements of dtype
+ *   out  device, 1 element of dtype (written)
+ * Limit: inputs of at most 2^36 bytes (2^34 f32 or 2^33 f64 elements);
+ * larger n returns DET_ERR_TOO_LARGE and enqueues nothing.
+ * Set-up: the first call on a device (with that device current) looks up
+ * the device address of the static array once; make that first call before
+ * any stream capture.  The call allocates nothing and frees nothing.
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's contents (each call clears the part that must start at zero).
+ * Calls whose work can overlap on the GPU -- different streams without
+ * ordering between them, or different host threads -- race on that array
+ * and must not be made.
+ */
+#define DET_SUM_NOALLOC_MAX_PARTIALS 16384
+int det_sum_noalloc(const void* x, int64_t n, int dtype, void* out, int block_threads, void* stream);
 
 /* ------------------------------------------------------------------------
  * det_scatter_add -- out[bins[i]] += values[i] for every i with
