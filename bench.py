@@ -56,24 +56,36 @@ def _np_dt(name):
     return {"f32": np.float32, "f64": np.float64}[name]
 
 
-def build_workload(name, torch, det, dev):
-    import oracle as _oracle_mod  # noqa: F401  (imported lazily by oracle_sample only)
-    tdt = {"f32": torch.float32, "f64": torch.float64}
+def _timed_oracle(fn, budget_s=3.0):
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        fn()
+        reps += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    return reps, time.perf_counter() - t0
 
-    if name in ("sum", "sum_f64", "sum_small", "sum_small_f64"):
-        dt = "f64" if name.endswith("f64") else "f32"
+
+def build_workload(name, torch, det, dev):
+    """Device-resident inputs and the step closures of one workload."""
+    tdt = {"f32": torch.float32, "f64": torch.float64}
+    dt = "f64" if name.endswith("f64") else "f32"
+    code = 0 if dt == "f32" else 1
+    npdt = _np_dt(dt)
+
+    if name.startswith("sum"):
         n = workloads.SUM_N if name.startswith("sum_small") else 1 << 28
-        x_np = workloads.sum_input(n=n, dtype=_np_dt(dt))
+        x_np = workloads.sum_input(n=n, dtype=npdt)
         x = torch.from_numpy(x_np).to(dev)
         out = torch.empty(1, dtype=tdt[dt], device=dev)
-        ws = det.workspace(det.lib().det_sum_workspace_bytes(n, 0 if dt == "f32" else 1), dev)
+        ws = det.workspace(det.lib().det_sum_workspace_bytes(n, code), dev)
         s = x_np.itemsize
+        host_x = torch.from_numpy(x_np).pin_memory()
+        host_out = torch.empty(1, dtype=tdt[dt]).pin_memory()
 
         def step():
             det.det_sum(x, out, workspace=ws)
-
-        host_x = torch.from_numpy(x_np).pin_memory()
-        host_out = torch.empty(1, dtype=tdt[dt]).pin_memory()
 
         def e2e_step():
             x.copy_(host_x, non_blocking=True)
@@ -83,24 +95,57 @@ def build_workload(name, torch, det, dev):
         def oracle_sample():
             import oracle
             m = min(n, 1 << 26)
-            xs = x_np[:m]
-            t0 = time.perf_counter()
-            reps = 0
-            while True:
-                oracle.det_sum(xs)
-                reps += 1
-                if time.perf_counter() - t0 > 3.0:
-                    break
-            return m * reps, time.perf_counter() - t0, f"{reps} x det_sum of the first {m} elements"
-
-        def result_bytes():
-            return out.cpu().numpy().tobytes()
+            reps, secs = _timed_oracle(lambda: oracle.det_sum(x_np[:m]))
+            return m * reps, secs, f"{reps} x det_sum of the first {m} elements, 1 thread"
 
         return dict(step=step, elems=n, algo_bytes=n * s, step_bytes=n * s, dominant="det_sum",
                     dtype=dt, e2e_step=e2e_step, h2d=n * s, d2h=s, oracle_sample=oracle_sample,
-                    result_bytes=result_bytes,
-                    config={"workload": f"det_sum n={n} uniform[0,12) {dt}", "n": n, "seed": 0,
+                    config={"workload": f"det_sum n={n} uniform[0,12) {dt} seed 0", "n": n,
                             "l2": "flushed between timed steps"})
+
+    if name.startswith("scan") or name.startswith("segscan"):
+        seg = name.startswith("segscan")
+        n = workloads.SCAN_SMALL_N if "small" in name else workloads.SCAN_N
+        x_np = workloads.scan_input(n=n, dtype=npdt)
+        x = torch.from_numpy(x_np).to(dev)
+        y = torch.empty_like(x)
+        s = x_np.itemsize
+        host_x = torch.from_numpy(x_np).pin_memory()
+        host_y = torch.empty_like(host_x).pin_memory()
+        if seg:
+            off_np = workloads.segment_offsets(n)
+            off = torch.from_numpy(off_np).to(dev)
+            ws = det.workspace(det.lib().det_segmented_scan_workspace_bytes(n, off.numel() - 1, code), dev)
+
+            def step():
+                det.det_segmented_scan(x, off, y, workspace=ws)
+        else:
+            ws = det.workspace(det.lib().det_scan_workspace_bytes(n, code), dev)
+
+            def step():
+                det.det_scan(x, y, workspace=ws)
+
+        def e2e_step():
+            x.copy_(host_x, non_blocking=True)
+            step()
+            host_y.copy_(y, non_blocking=True)
+
+        def oracle_sample():
+            import oracle
+            m = min(n, 1 << 24)
+            if seg:
+                o = workloads.segment_offsets(m)
+                reps, secs = _timed_oracle(lambda: oracle.det_segmented_scan(x_np[:m], o))
+            else:
+                reps, secs = _timed_oracle(lambda: oracle.det_scan(x_np[:m]))
+            return m * reps, secs, f"{reps} x {'segmented ' if seg else ''}scan of the first {m} elements, 1 thread"
+
+        kern = "det_segmented_scan" if seg else "det_scan"
+        extra = " segments geometric(mean 4096)" if seg else ""
+        return dict(step=step, elems=n, algo_bytes=2 * n * s, step_bytes=2 * n * s, dominant=kern,
+                    dtype=dt, e2e_step=e2e_step, h2d=n * s, d2h=n * s, oracle_sample=oracle_sample,
+                    config={"workload": f"{kern} forward inclusive n={n} lognormal(0,1) {dt} seed 4{extra}",
+                            "n": n, "l2": "inputs and outputs larger than L2; L2 flushed between timed steps"})
 
     raise SystemExit(f"unknown workload {name}")
 
@@ -321,12 +366,22 @@ def ref_dtype(name):
 def ref_sample(name):
     """One bounded oracle step of the workload: (elements, seconds, description)."""
     import oracle
+    npdt = _np_dt(ref_dtype(name))
     if name.startswith("sum"):
         n = 1 << 24
-        x = workloads.sum_input(n=n, dtype=_np_dt(ref_dtype(name)))
+        x = workloads.sum_input(n=n, dtype=npdt)
         t0 = time.perf_counter()
         oracle.det_sum(x)
         return n, time.perf_counter() - t0, f"det_sum of {n} elements"
+    if name.startswith("scan") or name.startswith("segscan"):
+        n = 1 << 22
+        x = workloads.scan_input(n=n, dtype=npdt)
+        t0 = time.perf_counter()
+        if name.startswith("segscan"):
+            oracle.det_segmented_scan(x, workloads.segment_offsets(n))
+        else:
+            oracle.det_scan(x)
+        return n, time.perf_counter() - t0, f"{name} of {n} elements"
     raise SystemExit(f"unknown workload {name}")
 
 

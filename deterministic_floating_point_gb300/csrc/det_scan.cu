@@ -1,0 +1,536 @@
+// det_scan / det_segmented_scan: single-pass decoupled look-back prefix sum
+// whose look-back is anchored, so the association order never depends on
+// which predecessors a chunk happens to observe as finished.
+//
+// drjit-core pull request "Make CUDA floating-point prefix sums
+// deterministic": "Root cause" (a block observing PARTIAL/INCLUSIVE states in
+// scheduling-dependent ways changes the association) and "Implementation"
+// (fixed warp-sized anchor intervals; each lane examines a fixed predecessor,
+// waits for the interval anchor's inclusive prefix, and a fixed-order warp
+// reduction runs through that anchor; only anchor chunks publish inclusive
+// prefixes).
+//
+// Frozen order (identical for every block size):
+//   chunk c       C = 32 virtual warps x 32 lanes x E elements (E = 32 f32,
+//                 16 f64); virtual lane (w, l) owns t = w*32E + l*E + e.
+//   lane          LT = in-lane fold x0 + x1 + ... (left to right)
+//   lanes         Kogge-Stone over l: K[l] = K[l-2^r] + K[l]; LX[l] = K[l-1]
+//   warps         the same over w on the warp totals: WX[w], Agg(c) = K[31]
+//   look-back     c = 32k + j; lane L reads Agg(c-1-L) for L < j and the
+//                 anchor prefix A(k-1) for L = j; Excl(c) = PT over lanes
+//   anchor        j = 31 publishes A(k) = Excl(c) + Agg(c)
+//   element       y = (Excl + WX[w]) + LX[l], then y = y + x_e for each e
+// Segmented: every '+' becomes (fa,a)(+)(fb,b) = (fa|fb, fb ? b : a+b) with
+// the earlier part as left operand.  Exclusive output is the inclusive
+// output shifted by one (first element +0.0; +0.0 at segment heads).
+// Reverse is the scan of the reversed input (and reversed segmentation).
+//
+// Execution: one CTA per chunk in ticket order (an integer atomic), so every
+// predecessor of a chunk has already started; the chunk is staged in shared
+// memory with 144-byte rows (one virtual lane per row, padded so that rows
+// read by a warp hit distinct banks); warp 0 does the look-back.  Every wait
+// has a time limit: on expiry the status word gets DET_ERR_LOOKBACK_TIMEOUT
+// and all later waits of the launch give up at once.
+#include "det_common.cuh"
+
+namespace det {
+namespace {
+
+template <typename T> struct Bits;
+template <> struct Bits<float> {
+  using U = unsigned int;
+  static constexpr U kSentinel = 0xffffffffu;
+  static constexpr U kQNaN = 0x7fc00000u;
+};
+template <> struct Bits<double> {
+  using U = unsigned long long;
+  static constexpr U kSentinel = 0xffffffffffffffffull;
+  static constexpr U kQNaN = 0x7ff8000000000000ull;
+};
+
+template <typename T> __device__ __forceinline__ typename Bits<T>::U to_bits(T v);
+template <> __device__ __forceinline__ unsigned int to_bits<float>(float v) { return __float_as_uint(v); }
+template <> __device__ __forceinline__ unsigned long long to_bits<double>(double v) {
+  return (unsigned long long)__double_as_longlong(v);
+}
+__device__ __forceinline__ float from_bits(unsigned int b) { return __uint_as_float(b); }
+__device__ __forceinline__ double from_bits(unsigned long long b) { return __longlong_as_double((long long)b); }
+
+__device__ __forceinline__ void st_relaxed(unsigned int* p, unsigned int v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int ld_relaxed(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Publish a value word.  The all-ones pattern marks "not yet published"; the
+// only value with those bits is a NaN, which is published as the canonical
+// quiet NaN instead (NaN payloads are outside the bit-exact promise).
+template <typename T>
+__device__ __forceinline__ void publish(typename Bits<T>::U* p, T v) {
+  typename Bits<T>::U b = to_bits<T>(v);
+  if (b == Bits<T>::kSentinel) b = Bits<T>::kQNaN;
+  st_relaxed(p, b);
+}
+
+// Wait (bounded in time) for a published value word.  Returns false if the
+// launch has given up (this wait timed out, or another one did).
+template <typename T>
+__device__ bool wait_value(const typename Bits<T>::U* p, T& out, unsigned int* status,
+                           unsigned long long timeout_ns) {
+  typename Bits<T>::U b = ld_relaxed(p);
+  if (b != Bits<T>::kSentinel) {
+    out = from_bits(b);
+    return true;
+  }
+  const unsigned long long t0 = globaltimer();
+  unsigned int polls = 0;
+  while (true) {
+    b = ld_relaxed(p);
+    if (b != Bits<T>::kSentinel) {
+      out = from_bits(b);
+      return true;
+    }
+    if ((++polls & 63u) == 0) {
+      if (ld_relaxed(status) != 0u) break;
+      if (globaltimer() - t0 > timeout_ns) {
+        set_status(status, DET_ERR_LOOKBACK_TIMEOUT);
+        break;
+      }
+    }
+  }
+  out = absent<T>();
+  return false;
+}
+
+// Segmented operator on (flag, value); a is the earlier part.
+template <typename T, bool SEG>
+__device__ __forceinline__ void segop(bool fa, T a, bool fb, T b, bool& fr, T& r) {
+  if (SEG) {
+    fr = fa | fb;
+    r = fb ? b : a + b;
+  } else {
+    fr = false;
+    r = a + b;
+  }
+}
+
+template <typename T> struct ScanGeom {
+  static constexpr int E = sizeof(T) == 4 ? 32 : 16;         // elements per virtual lane
+  static constexpr int C = 1024 * E;                          // elements per chunk
+  static constexpr int ROW = E + 16 / (int)sizeof(T);         // padded row (elements)
+  static constexpr size_t kStageBytes = (size_t)1024 * ROW * sizeof(T);
+};
+
+template <typename T> struct ScanArgs {
+  const T* x;
+  T* y;
+  long long n;
+  long long nchunks;
+  typename Bits<T>::U* desc;     // Agg(c)
+  typename Bits<T>::U* anchors;  // A(k)
+  typename Bits<T>::U* tails;    // last inclusive value of chunk c (exclusive scans)
+  const unsigned int* head_bits; // segmented: head bitmap over scan-order positions
+  const unsigned char* has_head; // segmented: chunk contains a head
+  unsigned int* ticket;
+  unsigned int* status;
+  T* total_out;
+  unsigned long long timeout_ns;
+};
+
+// Shared memory of one CTA (dynamic): stage rows, then the small arrays.
+template <typename T> struct ScanSmem {
+  T lx[1024];
+  unsigned int lxf[32];   // segmented flags of lx (bit l of word w)
+  T wt[32];
+  T wx[32];
+  unsigned int wtf, wxf;  // flags of wt / wx (bit w)
+  T excl;
+  int exclf;
+  long long chunk;
+  unsigned int heads[ScanGeom<T>::C / 32];
+};
+
+template <typename T, bool SEG, bool REV, bool EXCL>
+__global__ void __launch_bounds__(1024, 1) scan_kernel(ScanArgs<T> a) {
+  using G = ScanGeom<T>;
+  constexpr int E = G::E, C = G::C, ROW = G::ROW;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  T* stage = reinterpret_cast<T*>(smem_raw);
+  ScanSmem<T>& sm = *reinterpret_cast<ScanSmem<T>*>(smem_raw + G::kStageBytes);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthreads = blockDim.x, nwarps = nthreads >> 5, R = 32 / nwarps;
+
+  if (tid == 0) {
+    sm.chunk = (long long)atomicAdd(a.ticket, 1u);
+    sm.wtf = 0u;
+  }
+  __syncthreads();
+  const long long c = sm.chunk;
+  if (c >= a.nchunks) return;
+  const long long base = c * C;                      // scan-order position of element 0
+  const long long nvalid = min((long long)C, a.n - base);
+
+  // ---- stage the chunk: scan-order element t -> row t/E, column t%E
+  auto gidx = [&](long long t) -> long long { return REV ? a.n - 1 - (base + t) : base + t; };
+  const bool vec_in = !REV && nvalid == C && ((reinterpret_cast<uintptr_t>(a.x + base) & 15) == 0);
+  if (vec_in) {
+    constexpr int PER16 = 16 / sizeof(T);
+    for (int i = tid; i < C / PER16; i += nthreads) {
+      const int t = i * PER16;
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(a.x + base + t));
+      *reinterpret_cast<float4*>(stage + (t / E) * ROW + (t % E)) = v;
+    }
+  } else {
+    for (int t = tid; t < C; t += nthreads) {
+      T v = t < nvalid ? a.x[gidx(t)] : absent<T>();
+      stage[(t / E) * ROW + (t % E)] = v;
+    }
+  }
+  if (SEG) {
+    // head bits of this chunk (bit t of the chunk's window); the bitmap covers
+    // ceil(n/32) words, positions past n read as "no head"
+    const long long w0 = base / 32;
+    const long long nwords = (a.n + 31) / 32;
+    for (int i = tid; i < C / 32; i += nthreads)
+      sm.heads[i] = (w0 + i < nwords) ? a.head_bits[w0 + i] : 0u;
+  }
+  __syncthreads();
+  auto head = [&](int t) -> bool { return SEG && ((sm.heads[t >> 5] >> (t & 31)) & 1u); };
+
+  // ---- phase 1: lane folds, Kogge-Stone over lanes, per virtual warp
+  for (int r = 0; r < R; ++r) {
+    const int v = warp * R + r;
+    const T* row = stage + (v * 32 + lane) * ROW;
+    const int t0 = v * 32 * E + lane * E;
+    T acc = row[0];
+    bool f = head(t0);
+#pragma unroll
+    for (int e = 1; e < E; ++e) {
+      bool fr;
+      segop<T, SEG>(f, acc, head(t0 + e), row[e], fr, acc);
+      f = fr;
+    }
+    // inclusive Kogge-Stone over the 32 lanes
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      T o = __shfl_up_sync(0xffffffffu, acc, d);
+      bool of = __shfl_up_sync(0xffffffffu, (int)f, d);
+      if (lane >= d) {
+        bool fr;
+        segop<T, SEG>(of, o, f, acc, fr, acc);
+        f = fr;
+      }
+    }
+    T lx = __shfl_up_sync(0xffffffffu, acc, 1);
+    bool lxf = __shfl_up_sync(0xffffffffu, (int)f, 1);
+    if (lane == 0) {
+      lx = absent<T>();
+      lxf = false;
+    }
+    sm.lx[v * 32 + lane] = lx;
+    unsigned int fm = __ballot_sync(0xffffffffu, lxf);
+    if (lane == 31) {
+      sm.wt[v] = acc;
+      sm.lxf[v] = fm;
+    }
+    // the virtual warp's total carries the flag of lane 31's inclusive value
+    const unsigned int wf = __ballot_sync(0xffffffffu, f);
+    if (SEG && lane == 0 && ((wf >> 31) & 1u)) atomicOr(&sm.wtf, 1u << v);
+  }
+  __syncthreads();
+
+  // ---- chunk aggregate, publication, anchored look-back (warp 0)
+  if (warp == 0) {
+    T acc = sm.wt[lane];
+    bool f = SEG && ((sm.wtf >> lane) & 1u);
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      T o = __shfl_up_sync(0xffffffffu, acc, d);
+      bool of = __shfl_up_sync(0xffffffffu, (int)f, d);
+      if (lane >= d) {
+        bool fr;
+        segop<T, SEG>(of, o, f, acc, fr, acc);
+        f = fr;
+      }
+    }
+    T wx = __shfl_up_sync(0xffffffffu, acc, 1);
+    bool wxf = __shfl_up_sync(0xffffffffu, (int)f, 1);
+    if (lane == 0) {
+      wx = absent<T>();
+      wxf = false;
+    }
+    sm.wx[lane] = wx;
+    const unsigned int wxm = __ballot_sync(0xffffffffu, wxf);
+    const T agg = __shfl_sync(0xffffffffu, acc, 31);
+    const bool aggf = __shfl_sync(0xffffffffu, (int)f, 31);
+    if (lane == 0) {
+      sm.wxf = wxm;
+      publish<T>(a.desc + c, agg);
+    }
+    // look-back
+    const long long k = c / 32;
+    const int j = (int)(c % 32);
+    T v = absent<T>();
+    bool vf = false;
+    if (lane < j) {
+      const long long q = c - 1 - lane;
+      wait_value<T>(a.desc + q, v, a.status, a.timeout_ns);
+      vf = SEG && a.has_head[q];
+    } else if (lane == j && k > 0) {
+      wait_value<T>(a.anchors + (k - 1), v, a.status, a.timeout_ns);
+      vf = SEG;  // position 0 is a head, so every anchor prefix carries the flag
+    }
+    // PT over lanes; higher lanes hold earlier chunks (left operand)
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+      T o = __shfl_xor_sync(0xffffffffu, v, s);
+      bool of = __shfl_xor_sync(0xffffffffu, (int)vf, s);
+      bool fr;
+      if (lane & s)
+        segop<T, SEG>(vf, v, of, o, fr, v);
+      else
+        segop<T, SEG>(of, o, vf, v, fr, v);
+      vf = fr;
+    }
+    if (lane == 0) {
+      sm.excl = v;
+      sm.exclf = vf;
+      if (j == 31) {
+        T an;
+        bool anf;
+        segop<T, SEG>(vf, v, aggf, agg, anf, an);
+        publish<T>(a.anchors + k, an);
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- phase 2: element values, written back into the stage rows
+  const T excl = sm.excl;
+  const bool exclf = SEG && sm.exclf;
+  for (int r = 0; r < R; ++r) {
+    const int v = warp * R + r;
+    T* row = stage + (v * 32 + lane) * ROW;
+    const int t0 = v * 32 * E + lane * E;
+    bool f1;
+    T y;
+    segop<T, SEG>(exclf, excl, SEG && ((sm.wxf >> v) & 1u), sm.wx[v], f1, y);
+    bool f2;
+    segop<T, SEG>(f1, y, SEG && ((sm.lxf[v] >> lane) & 1u), sm.lx[v * 32 + lane], f2, y);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const T xe = row[e];
+      y = (SEG && head(t0 + e)) ? xe : y + xe;
+      row[e] = y;
+    }
+  }
+  __syncthreads();
+
+  // ---- outputs
+  const T* st = stage;
+  auto sval = [&](int t) -> T { return st[(t / E) * ROW + (t % E)]; };
+  if (EXCL && tid == 0 && c + 1 < a.nchunks) publish<T>(a.tails + c, sval(C - 1));
+  if (tid == 0 && a.total_out && base + nvalid == a.n) *a.total_out = sval((int)nvalid - 1);
+  if (!EXCL) {
+    const bool vec_out = !REV && nvalid == C && ((reinterpret_cast<uintptr_t>(a.y + base) & 15) == 0);
+    if (vec_out) {
+      constexpr int PER16 = 16 / sizeof(T);
+      for (int i = tid; i < C / PER16; i += nthreads) {
+        const int t = i * PER16;
+        const float4 v = *reinterpret_cast<const float4*>(stage + (t / E) * ROW + (t % E));
+        __stcs(reinterpret_cast<float4*>(a.y + base + t), v);
+      }
+    } else {
+      for (int t = tid; t < nvalid; t += nthreads) a.y[gidx(t)] = sval(t);
+    }
+  } else {
+    for (int t = tid + 1; t < nvalid; t += nthreads) a.y[gidx(t)] = (SEG && head(t)) ? T(0.0) : sval(t - 1);
+    if (tid == 0) {
+      T first = T(0.0);
+      if (c > 0 && !(SEG && head(0))) wait_value<T>(a.tails + (c - 1), first, a.status, a.timeout_ns);
+      a.y[gidx(0)] = first;
+    }
+  }
+}
+
+// Segment heads in scan order: a bitmap over positions and a per-chunk flag.
+template <int C, bool REV>
+__global__ void seg_heads_kernel(const long long* __restrict__ off, long long nseg, long long n,
+                                 unsigned int* __restrict__ bits, unsigned char* __restrict__ has_head,
+                                 unsigned int* __restrict__ status) {
+  const long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= nseg) return;
+  const long long lo = off[s], hi = off[s + 1];
+  if (lo < 0 || hi > n || hi < lo) {
+    set_status(status, DET_ERR_INVALID_ARG);
+    return;
+  }
+  if (s == 0 && lo != 0) set_status(status, DET_ERR_INVALID_ARG);
+  if (s == nseg - 1 && hi != n) set_status(status, DET_ERR_INVALID_ARG);
+  if (lo == hi) return;
+  const long long h = REV ? n - hi : lo;
+  atomicOr(bits + (h >> 5), 1u << (h & 31));
+  has_head[h / C] = 1;
+}
+
+}  // namespace
+
+template <typename T> struct ScanWs {
+  size_t desc, anchors, tails, bits, has_head, total;
+};
+
+template <typename T>
+static ScanWs<T> scan_ws_layout(long long n, bool seg) {
+  using U = typename Bits<T>::U;
+  const long long C = ScanGeom<T>::C;
+  const long long nch = (n + C - 1) / C;
+  ScanWs<T> w;
+  size_t off = kHeaderBytes;
+  w.desc = off;
+  off = align_up(off + (size_t)(nch + 1) * sizeof(U), 256);
+  w.anchors = off;
+  off = align_up(off + (size_t)(nch / 32 + 2) * sizeof(U), 256);
+  w.tails = off;
+  off = align_up(off + (size_t)(nch + 1) * sizeof(U), 256);
+  w.bits = off;
+  if (seg) off = align_up(off + (size_t)((n + 31) / 32 + 1) * 4, 256);
+  w.has_head = off;
+  if (seg) off = align_up(off + (size_t)nch + 1, 256);
+  w.total = off;
+  return w;
+}
+
+template <typename T, bool SEG, bool REV, bool EXCL>
+static cudaError_t launch_scan(const ScanArgs<T>& a, int threads, cudaStream_t s) {
+  const size_t smem = ScanGeom<T>::kStageBytes + sizeof(ScanSmem<T>);
+  auto kern = scan_kernel<T, SEG, REV, EXCL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  launch_begin(SEG ? "det_segmented_scan" : "det_scan", s);
+  kern<<<(unsigned)a.nchunks, threads, smem, s>>>(a);
+  launch_end(s);
+  return cudaGetLastError();
+}
+
+template <typename T, bool SEG>
+static int scan_impl(const T* x, T* y, long long n, const long long* seg_off, long long nseg, int flags,
+                     T* total_out, void* ws, size_t ws_bytes, int bt, cudaStream_t s) {
+  const ScanWs<T> L = scan_ws_layout<T>(n, SEG);
+  if (ws_bytes < L.total) return DET_ERR_WORKSPACE;
+  char* w = reinterpret_cast<char*>(ws);
+  if (cudaMemsetAsync(w, 0, kHeaderBytes, s) != cudaSuccess) return DET_ERR_CUDA;
+  if (n == 0) {
+    if (total_out && cudaMemsetAsync(total_out, 0, sizeof(T), s) != cudaSuccess) return DET_ERR_CUDA;
+    return DET_OK;
+  }
+  if (cudaMemsetAsync(w + L.desc, 0xff, L.bits - L.desc, s) != cudaSuccess) return DET_ERR_CUDA;
+  WsHeader* h = reinterpret_cast<WsHeader*>(ws);
+  ScanArgs<T> a;
+  a.x = x;
+  a.y = y;
+  a.n = n;
+  a.nchunks = (n + ScanGeom<T>::C - 1) / ScanGeom<T>::C;
+  a.desc = reinterpret_cast<typename Bits<T>::U*>(w + L.desc);
+  a.anchors = reinterpret_cast<typename Bits<T>::U*>(w + L.anchors);
+  a.tails = reinterpret_cast<typename Bits<T>::U*>(w + L.tails);
+  a.head_bits = nullptr;
+  a.has_head = nullptr;
+  a.ticket = &h->ticket;
+  a.status = &h->status;
+  a.total_out = total_out;
+  a.timeout_ns = 2000000000ull;
+  const bool rev = flags & DET_SCAN_REVERSE, excl = flags & DET_SCAN_EXCLUSIVE;
+  if (SEG) {
+    if (cudaMemsetAsync(w + L.bits, 0, L.total - L.bits, s) != cudaSuccess) return DET_ERR_CUDA;
+    unsigned int* bits = reinterpret_cast<unsigned int*>(w + L.bits);
+    unsigned char* hh = reinterpret_cast<unsigned char*>(w + L.has_head);
+    a.head_bits = bits;
+    a.has_head = hh;
+    if (nseg > 0) {
+      const unsigned blocks = (unsigned)((nseg + 255) / 256);
+      launch_begin("det_seg_heads", s);
+      if (rev)
+        seg_heads_kernel<ScanGeom<T>::C, true><<<blocks, 256, 0, s>>>(seg_off, nseg, n, bits, hh, &h->status);
+      else
+        seg_heads_kernel<ScanGeom<T>::C, false><<<blocks, 256, 0, s>>>(seg_off, nseg, n, bits, hh, &h->status);
+      launch_end(s);
+      if (cudaGetLastError() != cudaSuccess) return DET_ERR_CUDA;
+    }
+  }
+  const int threads = bt ? bt : 1024;
+  cudaError_t e;
+  if (rev) {
+    e = excl ? launch_scan<T, SEG, true, true>(a, threads, s) : launch_scan<T, SEG, true, false>(a, threads, s);
+  } else {
+    e = excl ? launch_scan<T, SEG, false, true>(a, threads, s) : launch_scan<T, SEG, false, false>(a, threads, s);
+  }
+  return e == cudaSuccess ? DET_OK : DET_ERR_CUDA;
+}
+
+}  // namespace det
+
+using namespace det;
+
+extern "C" size_t det_scan_workspace_bytes(int64_t n, int dtype) {
+  if (n < 0 || !valid_dtype(dtype)) return 0;
+  return dtype == DET_F32 ? scan_ws_layout<float>(n, false).total : scan_ws_layout<double>(n, false).total;
+}
+
+extern "C" size_t det_segmented_scan_workspace_bytes(int64_t n, int64_t num_segments, int dtype) {
+  if (n < 0 || num_segments < 0 || !valid_dtype(dtype)) return 0;
+  return dtype == DET_F32 ? scan_ws_layout<float>(n, true).total : scan_ws_layout<double>(n, true).total;
+}
+
+extern "C" int det_scan(const void* x, void* y, int64_t n, int dtype, int flags, void* total_out,
+                        void* workspace, size_t workspace_bytes, int block_threads, void* stream) {
+  if (!valid_dtype(dtype)) return DET_ERR_DTYPE;
+  if (n < 0 || !workspace || (n > 0 && (!x || !y)) || (flags & ~3) || !valid_block_threads(block_threads))
+    return DET_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256) return DET_ERR_WORKSPACE;
+  if (n > 0 && x != y) {
+    const char *xb = (const char*)x, *yb = (const char*)y;
+    const size_t bytes = (size_t)n * elem_size(dtype);
+    if (xb < yb + bytes && yb < xb + bytes) return DET_ERR_INVALID_ARG;  // partial overlap
+  }
+  if (dtype == DET_F32)
+    return scan_impl<float, false>((const float*)x, (float*)y, n, nullptr, 0, flags, (float*)total_out,
+                                   workspace, workspace_bytes, block_threads, as_stream(stream));
+  return scan_impl<double, false>((const double*)x, (double*)y, n, nullptr, 0, flags, (double*)total_out,
+                                  workspace, workspace_bytes, block_threads, as_stream(stream));
+}
+
+extern "C" int det_segmented_scan(const void* x, void* y, int64_t n, const int64_t* seg_offsets,
+                                  int64_t num_segments, int dtype, int flags, void* workspace,
+                                  size_t workspace_bytes, int block_threads, void* stream) {
+  if (!valid_dtype(dtype)) return DET_ERR_DTYPE;
+  if (n < 0 || num_segments < 0 || !workspace || (flags & ~3) || !valid_block_threads(block_threads))
+    return DET_ERR_INVALID_ARG;
+  if (n > 0 && (!x || !y || !seg_offsets || num_segments < 1)) return DET_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256) return DET_ERR_WORKSPACE;
+  if (n > 0 && x != y) {
+    const char *xb = (const char*)x, *yb = (const char*)y;
+    const size_t bytes = (size_t)n * elem_size(dtype);
+    if (xb < yb + bytes && yb < xb + bytes) return DET_ERR_INVALID_ARG;
+  }
+  if (dtype == DET_F32)
+    return scan_impl<float, true>((const float*)x, (float*)y, n, (const long long*)seg_offsets, num_segments,
+                                  flags, nullptr, workspace, workspace_bytes, block_threads, as_stream(stream));
+  return scan_impl<double, true>((const double*)x, (double*)y, n, (const long long*)seg_offsets, num_segments,
+                                 flags, nullptr, workspace, workspace_bytes, block_threads, as_stream(stream));
+}
