@@ -147,6 +147,54 @@ def build_workload(name, torch, det, dev):
                     config={"workload": f"{kern} forward inclusive n={n} lognormal(0,1) {dt} seed 4{extra}",
                             "n": n, "l2": "inputs and outputs larger than L2; L2 flushed between timed steps"})
 
+    if name.startswith("scatter") or name.startswith("skew"):
+        skew = name.startswith("skew")
+        if skew:
+            values_np, bins_np, out0_np = workloads.skewed_scatter_input(dtype=npdt)
+            wdesc = (f"det_scatter_add n={values_np.size} N(0,1) {dt}, Zipf(1.1) bins over {out0_np.size}, "
+                     f"5% out of range, seed 3")
+        else:
+            bin0 = "bin0" in name
+            values_np, bins_np, out0_np = workloads.scatter_input(dtype=npdt, all_in_bin0=bin0)
+            wdesc = (f"det_scatter_add n={values_np.size} N(0,1) {dt}, "
+                     + ("all records in bin 0" if bin0 else f"{out0_np.size} uniform bins") + ", seed 2")
+        n, m = values_np.size, out0_np.size
+        v = torch.from_numpy(values_np).to(dev)
+        b = torch.from_numpy(bins_np).to(dev)
+        out = torch.from_numpy(out0_np).to(dev)
+        ws = det.workspace(det.lib().det_scatter_add_workspace_bytes(n, m, code), dev)
+        s = values_np.itemsize
+        host_v = torch.from_numpy(values_np).pin_memory()
+        host_b = torch.from_numpy(bins_np).pin_memory()
+        host_out = torch.empty_like(out, device="cpu").pin_memory()
+        passes = 1 if m <= 1024 else 2
+
+        def step():
+            det.det_scatter_add(out, b, v, workspace=ws)
+
+        def e2e_step():
+            v.copy_(host_v, non_blocking=True)
+            b.copy_(host_b, non_blocking=True)
+            det.det_scatter_add(out, b, v, workspace=ws)
+            host_out.copy_(out, non_blocking=True)
+
+        def oracle_sample():
+            import oracle
+            k = min(n, 1 << 22)
+            reps, secs = _timed_oracle(lambda: oracle.det_scatter_add(out0_np, bins_np[:k], values_np[:k]))
+            return k * reps, secs, f"{reps} x det_scatter_add of the first {k} records, 1 thread"
+
+        # one sort pass reads key + value and writes value (+ key between passes)
+        pass_bytes = n * (4 + s + s + (4 if passes > 1 else 0))
+        if passes == 1:
+            step_bytes = n * (4 + (4 + s) + s + s) + 2 * m * s        # hist, pass, tree, out
+        else:
+            step_bytes = n * (4 + 2 * (4 + s) + 2 * (4 + s) + 4 + s) + 2 * m * s
+        return dict(step=step, elems=n, algo_bytes=pass_bytes, step_bytes=step_bytes, dominant="det_sort_pass",
+                    dtype=dt, e2e_step=e2e_step, h2d=n * (4 + s), d2h=m * s, oracle_sample=oracle_sample,
+                    config={"workload": wdesc, "n": n, "bins": m, "sort_passes": passes,
+                            "l2": "L2 flushed between timed steps"})
+
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -373,6 +421,15 @@ def ref_sample(name):
         t0 = time.perf_counter()
         oracle.det_sum(x)
         return n, time.perf_counter() - t0, f"det_sum of {n} elements"
+    if name.startswith("scatter") or name.startswith("skew"):
+        k = 1 << 22
+        if name.startswith("skew"):
+            values, bins, out0 = workloads.skewed_scatter_input(n=k, dtype=npdt)
+        else:
+            values, bins, out0 = workloads.scatter_input(n=k, dtype=npdt, all_in_bin0="bin0" in name)
+        t0 = time.perf_counter()
+        oracle.det_scatter_add(out0, bins, values)
+        return k, time.perf_counter() - t0, f"{name}: det_scatter_add of {k} records"
     if name.startswith("scan") or name.startswith("segscan"):
         n = 1 << 22
         x = workloads.scan_input(n=n, dtype=npdt)
@@ -391,7 +448,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="det", choices=["det", "reference"])
-    ap.add_argument("--workload", default="sum")
+    ap.add_argument("--workload", default="scatter")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -59,5 +59,7 @@ def test_host_argument_checks_need_no_gpu(lib):
 
 def test_workspace_queries_are_host_only(lib):
     assert lib.det_sum_workspace_bytes(0, 0) >= 256
-    assert lib.det_sum_workspace_bytes(1 << 28, 0) > lib.det_sum_workspace_bytes(1 << 20, 0)
+    assert lib.det_sum_workspace_bytes(1 << 36, 0) > lib.det_sum_workspace_bytes(1 << 20, 0)
+    assert lib.det_scan_workspace_bytes(1 << 28, 0) > lib.det_scan_workspace_bytes(1 << 20, 0)
+    assert lib.det_scatter_add_workspace_bytes(1 << 24, 1024, 0) > 4 * (1 << 24)
     assert lib.det_sum_workspace_bytes(-1, 0) == 0
