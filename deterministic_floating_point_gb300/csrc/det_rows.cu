@@ -1,0 +1,164 @@
+// det_scatter_add_rows: deterministic form of the tile row scatter of
+// "warp.tile_atomic_add_indexed" along axis 0.
+//
+// The page's primitive adds element c of the tile to a[offset + indices[c_0],
+// c_1] atomically, skips destinations outside the array, lets repeated
+// indices accumulate and returns each destination's previous value -- with
+// the order (and so the rounding and the returned values) unspecified under
+// repeats.  Here:
+//   1. the row indices are sorted stably (payload: the source row id), so
+//      the rows aimed at one destination are in ascending source order;
+//   2. one warp per destination row reduces those rows column by column with
+//      the pairwise tree over their rank (rounds of 8 rows in registers,
+//      a binary counter across rounds), reads the old row once, writes it to
+//      prev for every contributor, and stores old + tree;
+//   3. skipped source rows get prev = +0.0.
+#include "det_sort.cuh"
+
+namespace det {
+namespace {
+
+constexpr int kCPL = 2;   // columns per lane per pass over the row (64 columns per warp pass)
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+rows_kernel(T* __restrict__ dst, long long R, long long W, const T* __restrict__ src, const int32_t* __restrict__ perm,
+            const int32_t* __restrict__ seg, const unsigned int* __restrict__ n_valid, T* __restrict__ prev,
+            long long src_rows) {
+  const long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= R) return;
+  const long long N = *n_valid;
+  const long long hi = min((long long)seg[r + 1], N), lo = max(0LL, min((long long)seg[r], hi));
+  const long long L = hi - lo;
+  if (L <= 0) return;
+  for (long long c0 = 0; c0 < W; c0 += 32 * kCPL) {
+    long long col[kCPL];
+    bool cok[kCPL];
+#pragma unroll
+    for (int c = 0; c < kCPL; ++c) {
+      col[c] = c0 + c * 32 + lane;
+      cok[c] = col[c] < W;
+    }
+    T stack[kCPL][40];
+    long long cnt = 0;
+    for (long long k0 = 0; k0 < L; k0 += 8) {
+      T v[kCPL][8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const bool in = k0 + e < L;
+        long long s = in ? (long long)perm[lo + k0 + e] : 0;
+        if (s < 0 || s >= src_rows) s = 0;   // cannot happen for a correct sort
+#pragma unroll
+        for (int c = 0; c < kCPL; ++c) v[c][e] = (in && cok[c]) ? __ldg(src + s * W + col[c]) : absent<T>();
+      }
+      T node[kCPL];
+#pragma unroll
+      for (int c = 0; c < kCPL; ++c) node[c] = thread_pt(v[c]);   // 8 rows -> level-3 node
+      int lvl = 0;
+      long long q = cnt;
+      while (q & 1) {
+#pragma unroll
+        for (int c = 0; c < kCPL; ++c) node[c] = stack[c][lvl] + node[c];
+        q >>= 1;
+        ++lvl;
+      }
+#pragma unroll
+      for (int c = 0; c < kCPL; ++c) stack[c][lvl] = node[c];
+      ++cnt;
+    }
+    T tree[kCPL];
+#pragma unroll
+    for (int c = 0; c < kCPL; ++c) {
+      bool have = false;
+      tree[c] = absent<T>();
+      for (int lvl = 0; lvl < 40; ++lvl) {
+        if ((cnt >> lvl) & 1) {
+          tree[c] = have ? stack[c][lvl] + tree[c] : stack[c][lvl];
+          have = true;
+        }
+      }
+    }
+    T old[kCPL];
+#pragma unroll
+    for (int c = 0; c < kCPL; ++c) old[c] = cok[c] ? dst[r * W + col[c]] : T(0);
+    if (prev) {
+      for (long long k = 0; k < L; ++k) {
+        long long s = perm[lo + k];
+        if (s < 0 || s >= src_rows) continue;
+#pragma unroll
+        for (int c = 0; c < kCPL; ++c)
+          if (cok[c]) prev[s * W + col[c]] = old[c];
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < kCPL; ++c)
+      if (cok[c]) dst[r * W + col[c]] = old[c] + tree[c];
+  }
+}
+
+// prev = +0.0 for source rows whose destination is outside [0, R).
+template <typename T>
+__global__ void rows_prev_skipped_kernel(const int32_t* __restrict__ idx, long long src_rows, long long offset,
+                                         long long R, long long W, T* __restrict__ prev) {
+  const long long s = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (s >= src_rows) return;
+  const long long r = (long long)idx[s] + offset;
+  if (r >= 0 && r < R) return;
+  for (long long j = lane; j < W; j += 32) prev[s * W + j] = T(0);
+}
+
+}  // namespace
+}  // namespace det
+
+using namespace det;
+
+extern "C" size_t det_scatter_add_rows_workspace_bytes(int64_t src_rows, int64_t dst_rows, int64_t row_len,
+                                                       int dtype) {
+  if (src_rows < 0 || dst_rows < 0 || row_len < 0 || !valid_dtype(dtype)) return 0;
+  return make_sort_plan(src_rows, dst_rows, 0, true, 128).total;
+}
+
+template <typename T>
+static int rows_impl(T* dst, long long R, long long W, const int32_t* idx, long long off, const T* src, long long M,
+                     T* prev, void* ws, size_t ws_bytes, int bt, cudaStream_t s) {
+  const SortPlan p = make_sort_plan(M, R, 0, true, bt);
+  if (ws_bytes < p.total) return DET_ERR_WORKSPACE;
+  if (M == 0 || W == 0) return cudaMemsetAsync(ws, 0, kHeaderBytes, s) == cudaSuccess ? DET_OK : DET_ERR_CUDA;
+  int fb = 0;
+  int rc = enqueue_sort(p, ws, idx, off, nullptr, nullptr, s, &fb);
+  if (rc != DET_OK) return rc;
+  char* w = reinterpret_cast<char*>(ws);
+  SortHdr* h = reinterpret_cast<SortHdr*>(ws);
+  if (prev) {
+    launch_begin("det_rows_prev_skipped", s);
+    rows_prev_skipped_kernel<T><<<(unsigned)((M * 32 + 255) / 256), 256, 0, s>>>(idx, M, off, R, W, prev);
+    launch_end(s);
+  }
+  if (R > 0) {
+    launch_begin("det_rows", s);
+    rows_kernel<T><<<(unsigned)((R * 32 + 255) / 256), 256, 0, s>>>(
+        dst, R, W, src, reinterpret_cast<const int32_t*>(w + p.idx[fb]), reinterpret_cast<const int32_t*>(w + p.seg),
+        &h->n_valid, prev, M);
+    launch_end(s);
+  }
+  return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
+}
+
+extern "C" int det_scatter_add_rows(void* dst, int64_t dst_rows, int64_t row_len, const int32_t* idx,
+                                    int64_t row_offset, const void* src, int64_t src_rows, void* prev_out, int dtype,
+                                    void* workspace, size_t workspace_bytes, int block_threads, void* stream) {
+  if (!valid_dtype(dtype)) return DET_ERR_DTYPE;
+  if (dst_rows < 0 || row_len < 0 || src_rows < 0 || !workspace || !valid_block_threads(block_threads))
+    return DET_ERR_INVALID_ARG;
+  if (src_rows > DET_MAX_RECORDS || dst_rows > 2147483647LL) return DET_ERR_TOO_LARGE;
+  if (src_rows > 0 && (!idx || (row_len > 0 && !src))) return DET_ERR_INVALID_ARG;
+  if (dst_rows > 0 && row_len > 0 && !dst) return DET_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256) return DET_ERR_WORKSPACE;
+  if (dtype == DET_F32)
+    return rows_impl<float>((float*)dst, dst_rows, row_len, idx, row_offset, (const float*)src, src_rows,
+                            (float*)prev_out, workspace, workspace_bytes, block_threads, as_stream(stream));
+  return rows_impl<double>((double*)dst, dst_rows, row_len, idx, row_offset, (const double*)src, src_rows,
+                           (double*)prev_out, workspace, workspace_bytes, block_threads, as_stream(stream));
+}

@@ -1,18 +1,15 @@
 // Stable LSD radix sort of (key, value, index) records with a validity
 // filter, and the segmented pairwise tree over the sorted values.
 //
-//   hist      one read of the keys: per-pass digit histograms of the valid
-//             keys (CTA-private shared counters, warp-aggregated with
-//             match.any, then integer atomics: order-free) and the valid count
-//   dstart    one CTA: exclusive scan of each pass's digit histogram
-//   pass p    per tile of K = threads * 32 records, in ticket order:
-//             warp multi-split ranks (match.any + popc) against per-warp
-//             shared counters give each record its rank among earlier records
-//             of its digit inside the warp; a cross-warp prefix per digit and
-//             an integer decoupled look-back over tiles (integer addition is
-//             associative, so whatever mix of partial and inclusive states a
-//             tile observes, the offsets are the same) give the global
-//             position digit_start + tile offset + warp offset + rank.
+//   count p   per tile of K = threads * 32 records: digit counts of the
+//             valid records (warp multi-split by ballots, one shared atomic
+//             per digit group: integer adds, order-free)
+//   colscan p per digit: exclusive prefix of the counts over tiles, and the
+//             digit totals (pass 0 also sums them into the valid count)
+//   pass p    per tile, independently: digit starts from the totals, warp
+//             multi-split ranks against per-warp shared counters give each
+//             record its rank among earlier records of its digit inside the
+//             warp; position = digit start + tile prefix + warp prefix + rank.
 //             Records keep their input order inside a digit: the pass is
 //             stable, so after the last pass each destination's records are
 //             in ascending original index.
@@ -27,94 +24,18 @@ namespace det {
 namespace {
 
 constexpr int kIPT = 32;                 // records per thread per tile
-constexpr unsigned long long kAggFlag = 1ull << 62;
-constexpr unsigned long long kInclFlag = 1ull << 63;
-constexpr unsigned long long kCountMask = (1ull << 40) - 1;
-
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-__device__ __forceinline__ unsigned long long gtimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024)
-sort_hist_kernel(const int32_t* __restrict__ keys, long long n, long long key_offset, long long m, int passes,
-                 int D, unsigned int* __restrict__ hist, unsigned int* __restrict__ n_valid) {
-  __shared__ unsigned int sh[4][1024];
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int ndig = 1 << D;
-  const unsigned mask = (unsigned)ndig - 1u;
-  for (int i = tid; i < 4 * 1024; i += blockDim.x) (&sh[0][0])[i] = 0u;
-  __syncthreads();
-  const long long nwarps_total = (long long)gridDim.x * (blockDim.x >> 5);
-  const long long gwarp = (long long)blockIdx.x * (blockDim.x >> 5) + (tid >> 5);
-  unsigned int local_valid = 0;
-  for (long long wb = gwarp * 32; wb < n; wb += nwarps_total * 32) {
-    const long long i = wb + lane;
-    const long long key = (i < n) ? (long long)keys[i] + key_offset : -1;
-    const bool valid = key >= 0 && key < m;
-    local_valid += valid;
-    for (int p = 0; p < passes; ++p) {
-      const unsigned d = ((unsigned)key >> (p * D)) & mask;
-      const unsigned peers = __match_any_sync(0xffffffffu, valid ? d : (0x80000000u | (unsigned)lane));
-      if (valid && lane == __ffs(peers) - 1) atomicAdd(&sh[p][d], (unsigned)__popc(peers));
-    }
+// Lanes of this warp whose (valid) digit equals mine, by one ballot per
+// digit bit (a warp multi-split); invalid lanes belong to no group.
+__device__ __forceinline__ unsigned digit_peers(unsigned d, bool valid, int D) {
+  unsigned peers = __ballot_sync(0xffffffffu, valid);
+  for (int b = 0; b < D; ++b) {
+    const bool bit = (d >> b) & 1u;
+    const unsigned bb = __ballot_sync(0xffffffffu, bit);
+    peers &= bit ? bb : ~bb;
   }
-  __syncthreads();
-  for (int p = 0; p < passes; ++p)
-    for (int d = tid; d < ndig; d += blockDim.x)
-      if (sh[p][d]) atomicAdd(&hist[p * 1024 + d], sh[p][d]);
-#pragma unroll
-  for (int s = 16; s > 0; s >>= 1) local_valid += __shfl_xor_sync(0xffffffffu, local_valid, s);
-  if (lane == 0 && local_valid) atomicAdd(n_valid, local_valid);
+  return peers;
 }
-
-// One CTA of 1024 threads: dstart[p][d] = sum of hist[p][d'] for d' < d.
-__global__ void __launch_bounds__(1024)
-sort_dstart_kernel(const unsigned int* __restrict__ hist, int passes, int D, unsigned int* __restrict__ dstart) {
-  __shared__ unsigned int wsum[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int ndig = 1 << D;
-  for (int p = 0; p < passes; ++p) {
-    const unsigned v = tid < ndig ? hist[p * 1024 + tid] : 0u;
-    unsigned x = v;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const unsigned o = __shfl_up_sync(0xffffffffu, x, d);
-      if (lane >= d) x += o;
-    }
-    if (lane == 31) wsum[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-      unsigned w = wsum[lane];
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const unsigned o = __shfl_up_sync(0xffffffffu, w, d);
-        if (lane >= d) w += o;
-      }
-      wsum[lane] = w;  // inclusive over warps
-    }
-    __syncthreads();
-    const unsigned before = (warp ? wsum[warp - 1] : 0u) + x - v;
-    if (tid < ndig) dstart[p * 1025 + tid] = before;
-    if (tid == ndig - 1) dstart[p * 1025 + ndig] = before + v;
-    __syncthreads();
-  }
-}
-
-template <int VB> struct Payload;
-template <> struct Payload<0> { using U = unsigned int; };
-template <> struct Payload<4> { using U = unsigned int; };
-template <> struct Payload<8> { using U = unsigned long long; };
 
 struct PassArgs {
   const int32_t* keys_in;
@@ -128,13 +49,144 @@ struct PassArgs {
   long long m;
   int shift;
   int D;
-  const unsigned int* dstart;
-  unsigned long long* state;
-  unsigned int* ticket;
+  long long tiles;
+  unsigned int* counts;        // [tiles][ndig]: tile counts, then exclusive column prefixes
+  unsigned int* totals;        // [ndig] column totals
   unsigned int* status;
-  const unsigned int* n_valid;
-  unsigned long long timeout_ns;
+  unsigned int* n_valid;
 };
+
+// Digit of record i of a pass, or 0xffffffff if it is past the end or
+// (first pass) its destination is outside [0, m).
+// The count kernel reads the keys with a normal cached load so that the
+// pass kernel, which reads them last, mostly finds them in L2.
+template <bool FIRST, bool LAST_USE>
+__device__ __forceinline__ unsigned record_digit(const PassArgs& a, long long i, long long N, unsigned mask) {
+  if (i >= N) return 0xffffffffu;
+  const int32_t raw = LAST_USE ? __ldcs(a.keys_in + i) : __ldg(a.keys_in + i);
+  if (FIRST) {
+    const long long k = (long long)raw + a.key_offset;
+    return (k >= 0 && k < a.m) ? ((unsigned)k >> a.shift) & mask : 0xffffffffu;
+  }
+  return ((unsigned)raw >> a.shift) & mask;
+}
+
+// counts[tile][d] = records of the tile with digit d.  Same tiling as the
+// scatter pass: K = blockDim.x * kIPT records, warp w owns a contiguous
+// 32 * kIPT slice.
+template <bool FIRST>
+__global__ void __launch_bounds__(1024) sort_count_kernel(PassArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned int* cnt = reinterpret_cast<unsigned int*>(smem_raw);   // [ndig]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ndig = 1 << a.D;
+  const unsigned mask = (unsigned)ndig - 1u;
+  const long long tile = blockIdx.x;
+  const long long N = FIRST ? a.n : (long long)*a.n_valid;
+  for (int d = tid; d < ndig; d += blockDim.x) cnt[d] = 0u;
+  __syncthreads();
+  const long long K = (long long)blockDim.x * kIPT;
+  const long long wbase = tile * K + (long long)warp * 32 * kIPT;
+  if (tile * K < N) {
+    unsigned dg[kIPT];
+#pragma unroll
+    for (int r = 0; r < kIPT; ++r) dg[r] = record_digit<FIRST, false>(a, wbase + (long long)r * 32 + lane, N, mask);
+#pragma unroll
+    for (int r = 0; r < kIPT; ++r) {
+      const bool valid = dg[r] != 0xffffffffu;
+      const unsigned peers = digit_peers(dg[r], valid, a.D);
+      if (valid && lane == __ffs(peers) - 1) atomicAdd(&cnt[dg[r]], (unsigned)__popc(peers));
+    }
+  }
+  __syncthreads();
+  for (int d = tid; d < ndig; d += blockDim.x) a.counts[tile * ndig + d] = cnt[d];
+}
+
+// For each digit column: exclusive prefix over tiles (in place) and the
+// column total.  CTA of 1024 threads = 32 digit lanes x 32 tile groups.
+__global__ void __launch_bounds__(1024) sort_colscan_kernel(PassArgs a, int count_valid) {
+  __shared__ unsigned int part[32][33];
+  const int dl = threadIdx.x & 31, g = threadIdx.x >> 5;
+  const int ndig = 1 << a.D;
+  const int d = blockIdx.x * 32 + dl;
+  const long long T = a.tiles;
+  const long long TG = (T + 31) / 32;
+  const long long t0 = g * TG, t1 = min(T, t0 + TG);
+  unsigned sum = 0;
+  if (d < ndig)
+    for (long long t = t0; t < t1; ++t) sum += a.counts[t * ndig + d];
+  part[g][dl] = sum;
+  __syncthreads();
+  if (g == 0) {
+    // exclusive scan over the 32 groups of column dl (serial: 32 adds)
+    unsigned run = 0;
+    for (int k = 0; k < 32; ++k) {
+      const unsigned v = part[k][dl];
+      part[k][dl] = run;
+      run += v;
+    }
+    if (d < ndig) a.totals[d] = run;
+    if (count_valid) {
+      unsigned tot = d < ndig ? run : 0u;
+#pragma unroll
+      for (int s = 16; s > 0; s >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, s);
+      if (dl == 0 && tot) atomicAdd(a.n_valid, tot);
+    }
+  }
+  __syncthreads();
+  unsigned run = part[g][dl];
+  if (d < ndig)
+    for (long long t = t0; t < t1; ++t) {
+      const unsigned v = a.counts[t * ndig + d];
+      a.counts[t * ndig + d] = run;
+      run += v;
+    }
+}
+
+// Exclusive block scan of the digit totals into base[0..ndig]; 1024 threads.
+__device__ __forceinline__ void digit_starts(const unsigned int* totals, int ndig, unsigned int* base,
+                                             unsigned int* wsum) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  const int per = (ndig + blockDim.x - 1) / blockDim.x;   // digits per thread (contiguous)
+  unsigned loc = 0;
+  for (int k = 0; k < per; ++k) {
+    const int d = tid * per + k;
+    if (d < ndig) loc += totals[d];
+  }
+  unsigned x = loc;
+#pragma unroll
+  for (int s = 1; s < 32; s <<= 1) {
+    const unsigned o = __shfl_up_sync(0xffffffffu, x, s);
+    if (lane >= s) x += o;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned wv = lane < nw ? wsum[lane] : 0u;
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+      const unsigned o = __shfl_up_sync(0xffffffffu, wv, s);
+      if (lane >= s) wv += o;
+    }
+    wsum[lane] = wv;
+  }
+  __syncthreads();
+  unsigned run = (warp ? wsum[warp - 1] : 0u) + x - loc;
+  for (int k = 0; k < per; ++k) {
+    const int d = tid * per + k;
+    if (d < ndig) {
+      base[d] = run;
+      run += totals[d];
+    }
+  }
+  if (tid == blockDim.x - 1) base[ndig] = run;
+  __syncthreads();
+}
+
+template <int VB> struct Payload;
+template <> struct Payload<0> { using U = unsigned int; };
+template <> struct Payload<4> { using U = unsigned int; };
+template <> struct Payload<8> { using U = unsigned long long; };
 
 template <int VB, bool FIRST, bool IDX, bool KEYS_OUT>
 __global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
@@ -143,40 +195,33 @@ __global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const int ndig = 1 << a.D;
   const unsigned mask = (unsigned)ndig - 1u;
-  unsigned short* wcnt = reinterpret_cast<unsigned short*>(smem_raw);                 // [nwarps][ndig]
-  unsigned int* gbase = reinterpret_cast<unsigned int*>(smem_raw + (size_t)nwarps * ndig * 2);  // [ndig]
-  __shared__ long long s_tile;
+  unsigned short* wcnt = reinterpret_cast<unsigned short*>(smem_raw);                          // [nwarps][ndig]
+  unsigned int* gbase = reinterpret_cast<unsigned int*>(smem_raw + (size_t)nwarps * ndig * 2);  // [ndig + 1]
+  __shared__ unsigned int wsum[32];
 
-  if (tid == 0) s_tile = (long long)atomicAdd(a.ticket, 1u);
-  __syncthreads();
-  const long long tile = s_tile;
+  const long long tile = blockIdx.x;
   const long long N = FIRST ? a.n : (long long)*a.n_valid;
   const long long K = (long long)blockDim.x * kIPT;
   const long long tile_base = tile * K;
   if (tile_base >= N) return;
   const long long wbase = tile_base + (long long)warp * 32 * kIPT;
 
+  // digit starts (from the column totals) plus this tile's column prefixes
+  digit_starts(a.totals, ndig, gbase, wsum);
+  for (int d = tid; d < ndig; d += blockDim.x) gbase[d] += a.counts[tile * ndig + d];
   for (int d = lane; d < ndig; d += 32) wcnt[warp * ndig + d] = 0;
   __syncwarp();
 
-  // ---- rank inside the warp, record order = (round, lane) = input order
+  // ---- load this warp's digits (all loads in flight), then rank inside the
+  // warp; record order = (round, lane) = input order
   unsigned packed[kIPT];
 #pragma unroll
+  for (int r = 0; r < kIPT; ++r) packed[r] = record_digit<FIRST, true>(a, wbase + (long long)r * 32 + lane, N, mask);
+#pragma unroll
   for (int r = 0; r < kIPT; ++r) {
-    const long long i = wbase + (long long)r * 32 + lane;
-    bool valid = i < N;
-    unsigned key = 0;
-    if (valid) {
-      if (FIRST) {
-        const long long k = (long long)a.keys_in[i] + a.key_offset;
-        valid = k >= 0 && k < a.m;
-        key = (unsigned)k;
-      } else {
-        key = (unsigned)a.keys_in[i];
-      }
-    }
-    const unsigned d = (key >> a.shift) & mask;
-    const unsigned peers = __match_any_sync(0xffffffffu, valid ? d : (0x80000000u | (unsigned)lane));
+    const bool valid = packed[r] != 0xffffffffu;
+    const unsigned d = packed[r];
+    const unsigned peers = digit_peers(d, valid, a.D);
     unsigned base = 0;
     if (valid) base = wcnt[warp * ndig + d];
     __syncwarp();
@@ -186,7 +231,7 @@ __global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
   }
   __syncthreads();
 
-  // ---- per digit: warp offsets, tile count, look-back over tiles
+  // ---- per digit: exclusive prefix over the warps of this tile
   for (int d = tid; d < ndig; d += blockDim.x) {
     unsigned run = 0;
     for (int w = 0; w < nwarps; ++w) {
@@ -194,40 +239,6 @@ __global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
       wcnt[w * ndig + d] = (unsigned short)run;
       run += c;
     }
-    unsigned long long* st = a.state + tile * ndig + d;
-    if (tile == 0) {
-      st_relaxed_u64(st, kInclFlag | run);
-      gbase[d] = a.dstart[d];
-      continue;
-    }
-    st_relaxed_u64(st, kAggFlag | run);
-    unsigned long long excl = 0;
-    long long t = tile - 1;
-    bool ok = true;
-    while (t >= 0) {
-      const unsigned long long* q = a.state + t * ndig + d;
-      unsigned long long v = ld_relaxed_u64(q);
-      if (v == 0) {
-        const unsigned long long t0 = gtimer();
-        unsigned polls = 0;
-        while ((v = ld_relaxed_u64(q)) == 0) {
-          if ((++polls & 63u) == 0) {
-            if (*(volatile unsigned int*)a.status != 0u) { ok = false; break; }
-            if (gtimer() - t0 > a.timeout_ns) {
-              set_status(a.status, DET_ERR_LOOKBACK_TIMEOUT);
-              ok = false;
-              break;
-            }
-          }
-        }
-        if (!ok) break;
-      }
-      excl += v & kCountMask;
-      if (v & kInclFlag) break;
-      --t;
-    }
-    st_relaxed_u64(st, kInclFlag | (excl + run));
-    gbase[d] = a.dstart[d] + (unsigned)excl;
   }
   __syncthreads();
 
@@ -251,6 +262,15 @@ __global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
   }
 }
 
+// seg[0..m] = exclusive scan of the digit totals of a one-pass sort.
+__global__ void __launch_bounds__(1024) sort_seg_from_totals_kernel(const unsigned int* __restrict__ totals, int ndig,
+                                                                   long long m, int32_t* __restrict__ seg) {
+  __shared__ unsigned int base[1025];
+  __shared__ unsigned int wsum[32];
+  digit_starts(totals, ndig, base, wsum);
+  for (long long b = threadIdx.x; b <= m; b += blockDim.x) seg[b] = (int32_t)base[b];
+}
+
 // seg[b] = first sorted position with key >= b, for b = 0..m (keys sorted).
 __global__ void sort_bounds_kernel(const int32_t* __restrict__ keys, const unsigned int* __restrict__ n_valid,
                                    long long m, int32_t* __restrict__ seg, long long n) {
@@ -262,10 +282,6 @@ __global__ void sort_bounds_kernel(const int32_t* __restrict__ keys, const unsig
   for (long long b = prev + 1; b <= cur; ++b) seg[b] = (int32_t)i;
 }
 
-__global__ void copy_u32_kernel(const unsigned int* __restrict__ src, int32_t* __restrict__ dst, long long count) {
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < count) dst[i] = (int32_t)src[i];
-}
 
 // ---------------------------------------------------------------------------
 // PT over p[0..len) by one warp: rounds of 256 (8 per lane, in-register tree,
@@ -393,12 +409,10 @@ SortPlan make_sort_plan(long long n, long long m, int value_bytes, bool need_idx
   p.tiles = (n + K - 1) / K;
   const long long ndig = 1LL << p.digit_bits;
   size_t off = kHeaderBytes;
-  p.hist = off;
-  off = align_up(off + 4 * 1024 * 4, 256);
-  p.dstart = off;
-  off = align_up(off + 4 * 1025 * 4, 256);
-  p.state = off;
-  off = align_up(off + (size_t)(p.tiles + 1) * ndig * 8, 256);
+  p.totals = off;
+  off = align_up(off + 1025 * 4, 256);
+  p.counts = off;
+  off = align_up(off + (size_t)(p.tiles + 1) * ndig * 4, 256);
   const int nb = p.passes > 1 ? 2 : 1;
   for (int b = 0; b < nb; ++b) {
     if (p.passes > 1) {
@@ -432,7 +446,7 @@ template <int VB>
 static cudaError_t launch_pass(const PassArgs& a, bool first, bool idx, bool keys_out, int threads, long long tiles,
                                cudaStream_t s) {
   const int ndig = 1 << a.D;
-  const size_t smem = (size_t)(threads / 32) * ndig * 2 + (size_t)ndig * 4;
+  const size_t smem = (size_t)(threads / 32) * ndig * 2 + (size_t)(ndig + 1) * 4;
   void (*k)(PassArgs) = nullptr;
 #define DET_PICK(F, I, KO) \
   if (first == F && idx == I && keys_out == KO) k = sort_pass_kernel<VB, F, I, KO>;
@@ -451,33 +465,19 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
                  int32_t* perm_out, cudaStream_t s, int* final_buf) {
   char* w = reinterpret_cast<char*>(ws);
   SortHdr* h = reinterpret_cast<SortHdr*>(ws);
-  // header + histograms are contiguous: one memset
-  if (cudaMemsetAsync(w, 0, p.dstart, s) != cudaSuccess) return DET_ERR_CUDA;
+  if (cudaMemsetAsync(w, 0, kHeaderBytes, s) != cudaSuccess) return DET_ERR_CUDA;
   *final_buf = (p.passes - 1) & 1;
+  int32_t* seg = reinterpret_cast<int32_t*>(w + p.seg);
   if (p.n == 0 || p.m == 0) {
-    if (cudaMemsetAsync(w + p.seg, 0, (size_t)(p.m + 1) * 4, s) != cudaSuccess) return DET_ERR_CUDA;
+    if (cudaMemsetAsync(seg, 0, (size_t)(p.m + 1) * 4, s) != cudaSuccess) return DET_ERR_CUDA;
     return DET_OK;
   }
-  unsigned int* hist = reinterpret_cast<unsigned int*>(w + p.hist);
-  unsigned int* dstart = reinterpret_cast<unsigned int*>(w + p.dstart);
-  {
-    long long blocks = min((long long)2 * 152, (p.n + 1023) / 1024);
-    if (blocks < 1) blocks = 1;
-    launch_begin("det_sort_hist", s);
-    sort_hist_kernel<<<(unsigned)blocks, 1024, 0, s>>>(keys, p.n, key_offset, p.m, p.passes, p.digit_bits, hist,
-                                                      &h->n_valid);
-    launch_end(s);
-    if (cudaGetLastError() != cudaSuccess) return DET_ERR_CUDA;
-    launch_begin("det_sort_dstart", s);
-    sort_dstart_kernel<<<1, 1024, 0, s>>>(hist, p.passes, p.digit_bits, dstart);
-    launch_end(s);
-    if (cudaGetLastError() != cudaSuccess) return DET_ERR_CUDA;
-  }
-  const long long ndig = 1LL << p.digit_bits;
+  const int ndig = 1 << p.digit_bits;
+  unsigned int* totals = reinterpret_cast<unsigned int*>(w + p.totals);
+  unsigned int* counts = reinterpret_cast<unsigned int*>(w + p.counts);
   for (int pass = 0; pass < p.passes; ++pass) {
     const bool first = pass == 0, last = pass == p.passes - 1;
     const int out = pass & 1, in = (pass - 1) & 1;
-    if (cudaMemsetAsync(w + p.state, 0, (size_t)p.tiles * ndig * 8, s) != cudaSuccess) return DET_ERR_CUDA;
     PassArgs a;
     a.keys_in = first ? keys : reinterpret_cast<const int32_t*>(w + p.keys[in]);
     a.vals_in = first ? values : (p.value_bytes ? w + p.vals[in] : nullptr);
@@ -490,12 +490,22 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
     a.m = p.m;
     a.shift = pass * p.digit_bits;
     a.D = p.digit_bits;
-    a.dstart = dstart + pass * 1025;
-    a.state = reinterpret_cast<unsigned long long*>(w + p.state);
-    a.ticket = &h->tickets[pass];
+    a.tiles = p.tiles;
+    a.counts = counts;
+    a.totals = totals;
     a.status = &h->status;
     a.n_valid = &h->n_valid;
-    a.timeout_ns = 2000000000ull;
+    const size_t csmem = (size_t)ndig * 4;
+    launch_begin("det_sort_count", s);
+    if (first)
+      sort_count_kernel<true><<<(unsigned)p.tiles, p.threads, csmem, s>>>(a);
+    else
+      sort_count_kernel<false><<<(unsigned)p.tiles, p.threads, csmem, s>>>(a);
+    launch_end(s);
+    launch_begin("det_sort_colscan", s);
+    sort_colscan_kernel<<<(unsigned)((ndig + 31) / 32), 1024, 0, s>>>(a, first ? 1 : 0);
+    launch_end(s);
+    if (cudaGetLastError() != cudaSuccess) return DET_ERR_CUDA;
     const bool keys_out = p.passes > 1;
     cudaError_t e;
     if (p.value_bytes == 8)
@@ -506,10 +516,9 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
       e = launch_pass<0>(a, first, p.need_idx, keys_out, p.threads, p.tiles, s);
     if (e != cudaSuccess) return DET_ERR_CUDA;
   }
-  int32_t* seg = reinterpret_cast<int32_t*>(w + p.seg);
   if (p.passes == 1) {
-    launch_begin("det_sort_seg_copy", s);
-    copy_u32_kernel<<<(unsigned)((p.m + 1 + 255) / 256), 256, 0, s>>>(dstart, seg, p.m + 1);
+    launch_begin("det_sort_seg", s);
+    sort_seg_from_totals_kernel<<<1, 1024, 0, s>>>(totals, ndig, p.m, seg);
     launch_end(s);
   } else {
     launch_begin("det_sort_bounds", s);

@@ -27,7 +27,7 @@ struct SortPlan {
   int value_bytes = 0;      // payload value size (0, 4 or 8)
   bool need_idx = false;    // carry the original index
   // workspace offsets (bytes from the workspace start)
-  size_t hist = 0, dstart = 0, state = 0, keys[2] = {0, 0}, vals[2] = {0, 0}, idx[2] = {0, 0};
+  size_t totals = 0, counts = 0, keys[2] = {0, 0}, vals[2] = {0, 0}, idx[2] = {0, 0};
   size_t seg = 0, blocks = 0, lsegs = 0, nodes = 0, total = 0;
   long long max_blocks = 0, max_lsegs = 0;
 };
@@ -35,7 +35,6 @@ struct SortPlan {
 // Header fields of a sort workspace (overlays the first 256 bytes).
 struct SortHdr {
   unsigned int status;
-  unsigned int tickets[4];
   unsigned int n_valid;
   unsigned int long_blocks;
   unsigned int long_segs;
