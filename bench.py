@@ -32,6 +32,7 @@ sys.path.insert(0, ROOT)
 from deterministic_floating_point_gb300 import workloads  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
+BLOCK_THREADS = 0      # --block-threads: launch shape of the library calls (never changes the bits)
 
 
 def load_peaks():
@@ -67,6 +68,23 @@ def _timed_oracle(fn, budget_s=3.0):
     return reps, time.perf_counter() - t0
 
 
+def fingerprint(torch, *tensors):
+    """Exact fingerprint of result bits: SHA-256 of small results, a
+    position-weighted 64-bit integer sum of the bit patterns for large ones."""
+    import hashlib as _h
+    hs = _h.sha256()
+    for t in tensors:
+        nbytes = t.numel() * t.element_size()
+        if nbytes <= (64 << 20):
+            hs.update(t.detach().cpu().numpy().tobytes())
+        else:
+            bits = t.view(torch.int64 if t.element_size() == 8 else torch.int32).to(torch.int64)
+            g = torch.Generator(device=t.device).manual_seed(12345)
+            mult = torch.randint(1, 1 << 62, (bits.numel(),), generator=g, device=t.device, dtype=torch.int64) | 1
+            hs.update(str(int((bits.flatten() * mult).sum().item())).encode())
+    return hs.hexdigest()
+
+
 def build_workload(name, torch, det, dev):
     """Device-resident inputs and the step closures of one workload."""
     tdt = {"f32": torch.float32, "f64": torch.float64}
@@ -85,7 +103,7 @@ def build_workload(name, torch, det, dev):
         host_out = torch.empty(1, dtype=tdt[dt]).pin_memory()
 
         def step():
-            det.det_sum(x, out, workspace=ws)
+            det.det_sum(x, out, workspace=ws, block_threads=BLOCK_THREADS)
 
         def e2e_step():
             x.copy_(host_x, non_blocking=True)
@@ -98,7 +116,8 @@ def build_workload(name, torch, det, dev):
             reps, secs = _timed_oracle(lambda: oracle.det_sum(x_np[:m]))
             return m * reps, secs, f"{reps} x det_sum of the first {m} elements, 1 thread"
 
-        return dict(step=step, elems=n, algo_bytes=n * s, step_bytes=n * s, dominant="det_sum",
+        return dict(state={"x": x, "out": out}, step=step, elems=n, algo_bytes=n * s, step_bytes=n * s,
+                    dominant="det_sum",
                     dtype=dt, e2e_step=e2e_step, h2d=n * s, d2h=s, oracle_sample=oracle_sample,
                     config={"workload": f"det_sum n={n} uniform[0,12) {dt} seed 0", "n": n,
                             "l2": "flushed between timed steps"})
@@ -118,12 +137,12 @@ def build_workload(name, torch, det, dev):
             ws = det.workspace(det.lib().det_segmented_scan_workspace_bytes(n, off.numel() - 1, code), dev)
 
             def step():
-                det.det_segmented_scan(x, off, y, workspace=ws)
+                det.det_segmented_scan(x, off, y, workspace=ws, block_threads=BLOCK_THREADS)
         else:
             ws = det.workspace(det.lib().det_scan_workspace_bytes(n, code), dev)
 
             def step():
-                det.det_scan(x, y, workspace=ws)
+                det.det_scan(x, y, workspace=ws, block_threads=BLOCK_THREADS)
 
         def e2e_step():
             x.copy_(host_x, non_blocking=True)
@@ -142,7 +161,8 @@ def build_workload(name, torch, det, dev):
 
         kern = "det_segmented_scan" if seg else "det_scan"
         extra = " segments geometric(mean 4096)" if seg else ""
-        return dict(step=step, elems=n, algo_bytes=2 * n * s, step_bytes=2 * n * s, dominant=kern,
+        return dict(state={"x": x, "y": y}, step=step, elems=n, algo_bytes=2 * n * s, step_bytes=2 * n * s,
+                    dominant=kern,
                     dtype=dt, e2e_step=e2e_step, h2d=n * s, d2h=n * s, oracle_sample=oracle_sample,
                     config={"workload": f"{kern} forward inclusive n={n} lognormal(0,1) {dt} seed 4{extra}",
                             "n": n, "l2": "inputs and outputs larger than L2; L2 flushed between timed steps"})
@@ -170,7 +190,7 @@ def build_workload(name, torch, det, dev):
         passes = 1 if m <= 1024 else 2
 
         def step():
-            det.det_scatter_add(out, b, v, workspace=ws)
+            det.det_scatter_add(out, b, v, workspace=ws, block_threads=BLOCK_THREADS)
 
         def e2e_step():
             v.copy_(host_v, non_blocking=True)
@@ -190,10 +210,50 @@ def build_workload(name, torch, det, dev):
             step_bytes = n * (4 + (4 + s) + s + s) + 2 * m * s        # hist, pass, tree, out
         else:
             step_bytes = n * (4 + 2 * (4 + s) + 2 * (4 + s) + 4 + s) + 2 * m * s
-        return dict(step=step, elems=n, algo_bytes=pass_bytes, step_bytes=step_bytes, dominant="det_sort_pass",
+        return dict(state={"out": out, "out0": torch.from_numpy(out0_np).to(dev), "b": b, "v": v}, step=step,
+                    elems=n, algo_bytes=pass_bytes, step_bytes=step_bytes, dominant="det_sort_pass",
                     dtype=dt, e2e_step=e2e_step, h2d=n * (4 + s), d2h=m * s, oracle_sample=oracle_sample,
                     config={"workload": wdesc, "n": n, "bins": m, "sort_passes": passes,
                             "l2": "L2 flushed between timed steps"})
+
+    if name.startswith("rows"):
+        src_np, idx_np, dst0_np = workloads.rows_input(dtype=npdt)
+        M, W = src_np.shape
+        R = dst0_np.shape[0]
+        src = torch.from_numpy(src_np).to(dev)
+        idx = torch.from_numpy(idx_np).to(dev)
+        dst = torch.from_numpy(dst0_np).to(dev)
+        prev = torch.empty_like(src)
+        ws = det.workspace(det.lib().det_scatter_add_rows_workspace_bytes(M, R, W, code), dev)
+        s = src_np.itemsize
+        host_src = torch.from_numpy(src_np).pin_memory()
+        host_idx = torch.from_numpy(idx_np).pin_memory()
+        host_prev = torch.empty_like(host_src).pin_memory()
+
+        def step():
+            det.det_scatter_add_rows(dst, idx, src, prev_out=prev, workspace=ws, block_threads=BLOCK_THREADS)
+
+        def e2e_step():
+            src.copy_(host_src, non_blocking=True)
+            idx.copy_(host_idx, non_blocking=True)
+            det.det_scatter_add_rows(dst, idx, src, prev_out=prev, workspace=ws)
+            host_prev.copy_(prev, non_blocking=True)
+
+        def oracle_sample():
+            import oracle
+            k = 1 << 17
+            reps, secs = _timed_oracle(lambda: oracle.det_scatter_add_rows(dst0_np, idx_np[:k], src_np[:k]))
+            return k * W * reps, secs, f"{reps} x det_scatter_add_rows of the first {k} source rows, 1 thread"
+
+        rows_bytes = 2 * M * W * s + 2 * R * W * s + 4 * M    # src in, prev out, dst in/out, sorted ids
+        return dict(state={"dst": dst, "dst0": torch.from_numpy(dst0_np).to(dev), "idx": idx, "src": src,
+                           "prev": prev}, step=step, elems=M * W, algo_bytes=rows_bytes,
+                    step_bytes=rows_bytes + 12 * M,
+                    dominant="det_rows", dtype=dt, e2e_step=e2e_step, h2d=M * W * s + 4 * M, d2h=M * W * s,
+                    oracle_sample=oracle_sample,
+                    config={"workload": f"det_scatter_add_rows src {M}x{W} N(0,1) {dt}, rows uniform over {R}, "
+                                        "prev returned, seed 5", "src_rows": M, "dst_rows": R, "row_len": W,
+                            "l2": "inputs larger than L2; L2 flushed between timed steps"})
 
     raise SystemExit(f"unknown workload {name}")
 
@@ -262,6 +322,61 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 
+def add_checks(name, wl, torch, det, dev):
+    """Attach closures for determinism counting: det_once() and base_once()
+    run the deterministic call / its nondeterministic baseline from the same
+    initial state and return a fingerprint of the result bits."""
+    st = wl["state"]
+    if name.startswith("sum"):
+        x, out = st["x"], st["out"]
+        bout = torch.empty_like(out)
+        wl["det_once"] = lambda: (wl["step"](), fingerprint(torch, out))[1]
+        wl["base_once"] = lambda: (det.atomic_sum(x, bout), fingerprint(torch, bout))[1]
+        wl["base_step"] = lambda: det.atomic_sum(x, bout)
+        wl["base_name"] = "atomic_sum"
+    elif name.startswith("scatter") or name.startswith("skew"):
+        out, out0, b, v = st["out"], st["out0"], st["b"], st["v"]
+
+        def d1():
+            out.copy_(out0)
+            wl["step"]()
+            return fingerprint(torch, out)
+
+        def b1():
+            out.copy_(out0)
+            det.atomic_scatter_add(out, b, v)
+            return fingerprint(torch, out)
+        wl["det_once"], wl["base_once"] = d1, b1
+        wl["base_step"] = lambda: det.atomic_scatter_add(out, b, v)
+        wl["base_name"] = "atomic_scatter_add"
+    elif name.startswith("rows"):
+        dst, dst0, idx, src, prev = st["dst"], st["dst0"], st["idx"], st["src"], st["prev"]
+
+        def d1():
+            dst.copy_(dst0)
+            wl["step"]()
+            return fingerprint(torch, dst, prev)
+
+        def b1():
+            dst.copy_(dst0)
+            det.atomic_scatter_add_rows(dst, idx, src, prev_out=prev)
+            return fingerprint(torch, dst, prev)
+        wl["det_once"], wl["base_once"] = d1, b1
+        wl["base_step"] = lambda: det.atomic_scatter_add_rows(dst, idx, src, prev_out=prev)
+        wl["base_name"] = "atomic_scatter_add_rows"
+    elif name.startswith("scan") or name.startswith("segscan"):
+        x, y = st["x"], st["y"]
+        yb = torch.empty_like(y)
+        bws = det.workspace(det.lib().det_dlb_scan_workspace_bytes(x.numel(), 0 if x.dtype == torch.float32 else 1),
+                            dev)
+        wl["det_once"] = lambda: (wl["step"](), fingerprint(torch, y))[1]
+        if name.startswith("scan"):
+            wl["base_once"] = lambda: (det.dlb_scan(x, yb, bws), fingerprint(torch, yb))[1]
+            wl["base_step"] = lambda: det.dlb_scan(x, yb, bws)
+            wl["base_name"] = "dlb_scan (unmodified look-back)"
+    return wl
+
+
 def time_steps(torch, wl, steps, flush, timer_cls=None):
     """Per-step CUDA-event times (ms) with an L2 flush before each step."""
     stream = torch.cuda.current_stream()
@@ -305,6 +420,55 @@ def traffic_for(kernel, workload):
         return None
 
 
+OPS = ["sum", "sum_f64", "sum_small", "scatter_f64", "scatter_bin0", "skew", "skew_f32", "scan", "scan_f64",
+       "scan_small", "segscan", "rows"]
+
+
+def measure_op(name, torch, det, dev, flush, steps, runs, peak):
+    """One workload: device time per step, dominant-kernel roofline, the
+    baseline's time, and distinct result fingerprints over repeated runs."""
+    wl = add_checks(name, build_workload(name, torch, det, dev), torch, det, dev)
+    for _ in range(3):
+        wl["step"]()
+    torch.cuda.synchronize()
+    times, kernels = time_steps(torch, wl, steps, flush, det.KernelTimer)
+    per_kernel = {}
+    for step_k in kernels:
+        for kname, ms in step_k:
+            per_kernel.setdefault(kname, []).append(ms)
+    dom = wl["dominant"]
+    dom_ms = statistics.mean(per_kernel[dom]) if dom in per_kernel else None
+    ms = statistics.mean(times)
+    res = {"workload": wl["config"]["workload"], "dtype": wl["dtype"], "Gelem_s": wl["elems"] / (ms * 1e-3) / 1e9,
+           "ms_per_step": ms, "step_GB_s": wl["step_bytes"] / (ms * 1e-3) / 1e9,
+           "kernel": dom, "kernel_ms": dom_ms,
+           "kernel_GB_s": (wl["algo_bytes"] / (dom_ms * 1e-3) / 1e9) if dom_ms else None,
+           "kernel_frac_of_peak": (wl["algo_bytes"] / (dom_ms * 1e-3) / 1e9 / peak) if dom_ms else None,
+           "kernel_share": {k: round(sum(v) / sum(times), 4) for k, v in per_kernel.items()}}
+    res["distinct_results_det"] = len({wl["det_once"]() for _ in range(runs)})
+    if "base_once" in wl:
+        for _ in range(2):
+            wl["base_step"]()
+        torch.cuda.synchronize()
+        bt = []
+        for _ in range(steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            wl["base_step"]()
+            e1.record()
+            bt.append((e0, e1))
+        torch.cuda.synchronize()
+        bms = statistics.mean(a.elapsed_time(b) for a, b in bt)
+        res["baseline"] = {"name": wl["base_name"], "ms_per_step": bms,
+                           "Gelem_s": wl["elems"] / (bms * 1e-3) / 1e9,
+                           "det_over_baseline_time": ms / bms,
+                           "distinct_results": len({wl["base_once"]() for _ in range(runs)})}
+    del wl
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_det(args, torch, rank, world):
     from deterministic_floating_point_gb300 import det
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
@@ -334,6 +498,7 @@ def run_det(args, torch, rank, world):
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     value = world * wl["elems"] * args.steps / (total_ms * 1e-3) / 1e9
+    step_bytes = wl["step_bytes"]
 
     # dominant kernel: average launch duration over the timed steps
     per_kernel = {}
@@ -371,13 +536,30 @@ def run_det(args, torch, rank, world):
         cpu = {"value": elems / secs / 1e9, "unit": "Gelem/s", "cores": 1, "kind": "oracle",
                "sample": what}
 
+    dtype, config = wl["dtype"], dict(wl["config"], parallelism=f"replicas{world}")
+    ops = {}
+    if args.ops and rank == 0:
+        # the headline workload's own determinism count and baseline, then
+        # every other workload of the hot path, measured the same way
+        add_checks(args.workload, wl, torch, det, dev)
+        head = {"distinct_results_det": len({wl["det_once"]() for _ in range(args.runs)})}
+        if "base_once" in wl:
+            head["baseline"] = {"name": wl["base_name"],
+                                "distinct_results": len({wl["base_once"]() for _ in range(args.runs)})}
+        ops[args.workload] = head
+        del wl
+        torch.cuda.empty_cache()
+        for name in OPS:
+            if name != args.workload:
+                ops[name] = measure_op(name, torch, det, dev, flush, max(3, min(args.steps, 5)), args.runs, peak)
+
     line = {"metric": "Gelem/s and achieved HBM GB/s (% of GB300 HBM peak) for det sum/scatter/scan",
             "value": value, "unit": "Gelem/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": wl["dtype"], "data": "synthetic", "config": dict(wl["config"], parallelism=f"replicas{world}"),
+            "dtype": dtype, "data": "synthetic", "config": config,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
             "clocks": clk.summary(), "step_ms_min": min(times), "step_ms_median": statistics.median(times),
-            "algo_gbs_per_step": wl["step_bytes"] / (ms_per_step * 1e-3) / 1e9}
+            "algo_gbs_per_step": step_bytes / (ms_per_step * 1e-3) / 1e9, "ops": ops}
     return line
 
 
@@ -421,6 +603,12 @@ def ref_sample(name):
         t0 = time.perf_counter()
         oracle.det_sum(x)
         return n, time.perf_counter() - t0, f"det_sum of {n} elements"
+    if name.startswith("rows"):
+        k = 1 << 16
+        src, idx, dst0 = workloads.rows_input(src_rows=k, dtype=npdt)
+        t0 = time.perf_counter()
+        oracle.det_scatter_add_rows(dst0, idx, src)
+        return k * src.shape[1], time.perf_counter() - t0, f"det_scatter_add_rows of {k} source rows x 64"
     if name.startswith("scatter") or name.startswith("skew"):
         k = 1 << 22
         if name.startswith("skew"):
@@ -450,7 +638,13 @@ def main():
     ap.add_argument("--impl", default="det", choices=["det", "reference"])
     ap.add_argument("--workload", default="scatter")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--block-threads", type=int, default=0)
+    ap.add_argument("--no-ops", dest="ops", action="store_false",
+                    help="skip the other workloads measured beside the headline one")
+    ap.add_argument("--runs", type=int, default=10, help="repeated runs for the distinct-result counts")
     args = ap.parse_args()
+    global BLOCK_THREADS
+    BLOCK_THREADS = args.block_threads
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))

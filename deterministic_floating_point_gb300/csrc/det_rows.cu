@@ -101,12 +101,11 @@ rows_kernel(T* __restrict__ dst, long long R, long long W, const T* __restrict__
 template <typename T>
 __global__ void rows_prev_skipped_kernel(const int32_t* __restrict__ idx, long long src_rows, long long offset,
                                          long long R, long long W, T* __restrict__ prev) {
-  const long long s = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+  const long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= src_rows) return;
   const long long r = (long long)idx[s] + offset;
   if (r >= 0 && r < R) return;
-  for (long long j = lane; j < W; j += 32) prev[s * W + j] = T(0);
+  for (long long j = 0; j < W; ++j) prev[s * W + j] = T(0);
 }
 
 }  // namespace
@@ -133,7 +132,7 @@ static int rows_impl(T* dst, long long R, long long W, const int32_t* idx, long 
   SortHdr* h = reinterpret_cast<SortHdr*>(ws);
   if (prev) {
     launch_begin("det_rows_prev_skipped", s);
-    rows_prev_skipped_kernel<T><<<(unsigned)((M * 32 + 255) / 256), 256, 0, s>>>(idx, M, off, R, W, prev);
+    rows_prev_skipped_kernel<T><<<(unsigned)((M + 255) / 256), 256, 0, s>>>(idx, M, off, R, W, prev);
     launch_end(s);
   }
   if (R > 0) {

@@ -137,6 +137,39 @@ template <typename T> struct ScanGeom {
   static constexpr size_t kStageBytes = (size_t)1024 * ROW * sizeof(T);
 };
 
+// Copy one padded stage row (E elements, 16-byte aligned) into registers
+// with 16-byte shared loads; reversed order for reverse scans.
+template <typename T, int E, bool REVERSED>
+__device__ __forceinline__ void row_to_regs(const T* row, T (&x)[E]) {
+  constexpr int P = 16 / sizeof(T);
+#pragma unroll
+  for (int q = 0; q < E / P; ++q) {
+    const float4 v = reinterpret_cast<const float4*>(row)[q];
+    const T* pv = reinterpret_cast<const T*>(&v);
+#pragma unroll
+    for (int k = 0; k < P; ++k) {
+      if (REVERSED)
+        x[E - 1 - (q * P + k)] = pv[k];
+      else
+        x[q * P + k] = pv[k];
+    }
+  }
+}
+
+// Store E elements of a lane (32 B at a time, one full sector per lane per
+// instruction).  p must be 32-byte aligned.
+template <typename T, int E, bool REVERSED>
+__device__ __forceinline__ void regs_to_global_256(T* p, const T (&x)[E]) {
+  constexpr int P = 32 / sizeof(T);
+#pragma unroll
+  for (int q = 0; q < E / P; ++q) {
+    T v[P];
+#pragma unroll
+    for (int k = 0; k < P; ++k) v[k] = REVERSED ? x[E - 1 - (q * P + k)] : x[q * P + k];
+    st_256(p + q * P, v);
+  }
+}
+
 template <typename T> struct ScanArgs {
   const T* x;
   T* y;
@@ -148,6 +181,7 @@ template <typename T> struct ScanArgs {
   const unsigned int* head_bits; // segmented: head bitmap over scan-order positions
   const unsigned char* has_head; // segmented: chunk contains a head
   unsigned int* ticket;
+  unsigned int* role;             // first CTA to start runs the anchor chain
   unsigned int* status;
   T* total_out;
   unsigned long long timeout_ns;
@@ -166,6 +200,67 @@ template <typename T> struct ScanSmem {
   unsigned int heads[ScanGeom<T>::C / 32];
 };
 
+// The anchor chain, computed by one warp of one CTA of the launch.
+//
+// A(k) is the anchor chunk's own formula -- Excl(32k+31) + Agg(32k+31) with
+// Excl(32k+31) = PT over lanes of Agg(32k+30-L) for L < 31 and A(k-1) in lane
+// 31 -- so the bits are the same whoever computes it.  Holding A(k-1) in a
+// register, this warp only waits for each interval's aggregates (published
+// by the chunks without waiting on anything) instead of a cross-SM round
+// trip per interval; chunks read A(k-1) once from the published array.
+template <typename T, bool SEG>
+__device__ void anchor_chain(const ScanArgs<T>& a) {
+  using U = typename Bits<T>::U;
+  constexpr int kAhead = 4;                // intervals whose aggregates are loaded at once
+  const int lane = threadIdx.x & 31;
+  const long long nint = a.nchunks / 32;   // complete intervals
+  T prev = absent<T>();                    // A(k-1), in every lane
+  for (long long kb = 0; kb < nint; kb += kAhead) {
+    // lane L holds Agg(32k + L) of intervals kb .. kb+kAhead-1 (one round trip)
+    U b[kAhead];
+#pragma unroll
+    for (int q = 0; q < kAhead; ++q)
+      b[q] = (kb + q < nint) ? ld_relaxed(a.desc + 32 * (kb + q) + lane) : Bits<T>::kSentinel;
+#pragma unroll
+    for (int q = 0; q < kAhead; ++q) {
+      const long long k = kb + q;
+      if (k >= nint) break;
+      T mine;
+      if (b[q] != Bits<T>::kSentinel)
+        mine = from_bits(b[q]);
+      else
+        wait_value<T>(a.desc + 32 * k + lane, mine, a.status, a.timeout_ns);
+      const bool minef = SEG && a.has_head[32 * k + lane];
+      // tree lane t < 31 takes Agg(32k + 30 - t) (held by lane 30 - t); lane 31 takes A(k-1)
+      const int srcl = lane < 31 ? 30 - lane : 31;
+      T v = __shfl_sync(0xffffffffu, mine, srcl);
+      bool vf = __shfl_sync(0xffffffffu, (int)minef, srcl);
+      if (lane == 31) {
+        v = (k > 0) ? prev : absent<T>();
+        vf = SEG && k > 0;
+      }
+#pragma unroll
+      for (int s = 1; s < 32; s <<= 1) {
+        const T o = __shfl_xor_sync(0xffffffffu, v, s);
+        const bool of = __shfl_xor_sync(0xffffffffu, (int)vf, s);
+        bool fr;
+        if (lane & s)
+          segop<T, SEG>(vf, v, of, o, fr, v);
+        else
+          segop<T, SEG>(of, o, vf, v, fr, v);
+        vf = fr;
+      }
+      const T agg = __shfl_sync(0xffffffffu, mine, 31);
+      const bool aggf = __shfl_sync(0xffffffffu, (int)minef, 31);
+      T an;
+      bool anf;
+      segop<T, SEG>(vf, v, aggf, agg, anf, an);
+      if (lane == 0) publish<T>(a.anchors + k, an);
+      prev = an;
+    }
+  }
+}
+
 template <typename T, bool SEG, bool REV, bool EXCL>
 __global__ void __launch_bounds__(1024, 1) scan_kernel(ScanArgs<T> a) {
   using G = ScanGeom<T>;
@@ -177,11 +272,16 @@ __global__ void __launch_bounds__(1024, 1) scan_kernel(ScanArgs<T> a) {
   const int nthreads = blockDim.x, nwarps = nthreads >> 5, R = 32 / nwarps;
 
   if (tid == 0) {
-    sm.chunk = (long long)atomicAdd(a.ticket, 1u);
+    // the first CTA to start runs the anchor chain; the others take chunks
+    sm.chunk = atomicAdd(a.role, 1u) == 0u ? -1LL : (long long)atomicAdd(a.ticket, 1u);
     sm.wtf = 0u;
   }
   __syncthreads();
   const long long c = sm.chunk;
+  if (c < 0) {
+    if (warp == 0) anchor_chain<T, SEG>(a);
+    return;
+  }
   if (c >= a.nchunks) return;
   const long long base = c * C;                      // scan-order position of element 0
   const long long nvalid = min((long long)C, a.n - base);
@@ -216,14 +316,15 @@ __global__ void __launch_bounds__(1024, 1) scan_kernel(ScanArgs<T> a) {
   // ---- phase 1: lane folds, Kogge-Stone over lanes, per virtual warp
   for (int r = 0; r < R; ++r) {
     const int v = warp * R + r;
-    const T* row = stage + (v * 32 + lane) * ROW;
     const int t0 = v * 32 * E + lane * E;
-    T acc = row[0];
+    T xr[E];
+    row_to_regs<T, E, false>(stage + (v * 32 + lane) * ROW, xr);
+    T acc = xr[0];
     bool f = head(t0);
 #pragma unroll
     for (int e = 1; e < E; ++e) {
       bool fr;
-      segop<T, SEG>(f, acc, head(t0 + e), row[e], fr, acc);
+      segop<T, SEG>(f, acc, head(t0 + e), xr[e], fr, acc);
       f = fr;
     }
     // inclusive Kogge-Stone over the 32 lanes
@@ -311,13 +412,8 @@ __global__ void __launch_bounds__(1024, 1) scan_kernel(ScanArgs<T> a) {
     if (lane == 0) {
       sm.excl = v;
       sm.exclf = vf;
-      if (j == 31) {
-        T an;
-        bool anf;
-        segop<T, SEG>(vf, v, aggf, agg, anf, an);
-        publish<T>(a.anchors + k, an);
-      }
     }
+    (void)aggf;
   }
   __syncthreads();
 
@@ -333,12 +429,16 @@ __global__ void __launch_bounds__(1024, 1) scan_kernel(ScanArgs<T> a) {
     segop<T, SEG>(exclf, excl, SEG && ((sm.wxf >> v) & 1u), sm.wx[v], f1, y);
     bool f2;
     segop<T, SEG>(f1, y, SEG && ((sm.lxf[v] >> lane) & 1u), sm.lx[v * 32 + lane], f2, y);
+    T xr[E];
+    row_to_regs<T, E, false>(row, xr);
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      const T xe = row[e];
-      y = (SEG && head(t0 + e)) ? xe : y + xe;
-      row[e] = y;
+      y = (SEG && head(t0 + e)) ? xr[e] : y + xr[e];
+      xr[e] = y;
     }
+    constexpr int P = 16 / sizeof(T);
+#pragma unroll
+    for (int q = 0; q < E / P; ++q) reinterpret_cast<float4*>(row)[q] = reinterpret_cast<const float4*>(xr)[q];
   }
   __syncthreads();
 
@@ -366,6 +466,283 @@ __global__ void __launch_bounds__(1024, 1) scan_kernel(ScanArgs<T> a) {
       if (c > 0 && !(SEG && head(0))) wait_value<T>(a.tails + (c - 1), first, a.status, a.timeout_ns);
       a.y[gidx(0)] = first;
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Persistent variant for 1024-thread CTAs: one virtual lane per thread, the
+// current chunk held in registers, the next chunk (and its head bits)
+// prefetched into the padded shared stage with cp.async while the current
+// one publishes, looks back and writes.  Same association order as
+// scan_kernel, so the same bits.
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+template <typename T> struct KeepSmem {
+  T wt[32];
+  T wx[32];
+  T last[32];
+  unsigned int wtf, wxf;
+  T excl;
+  int exclf;
+  long long next;
+  alignas(16) unsigned int heads[2][ScanGeom<T>::C / 32];   // cp.async destinations: 16-byte aligned
+};
+
+template <typename T, bool SEG, bool REV, bool EXCL>
+__global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
+  using G = ScanGeom<T>;
+  constexpr int E = G::E, C = G::C, ROW = G::ROW, PER16 = 16 / (int)sizeof(T);
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  T* stage = reinterpret_cast<T*>(smem_raw);
+  KeepSmem<T>& sm = *reinterpret_cast<KeepSmem<T>*>(smem_raw + G::kStageBytes);
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int t0 = tid * E;   // first element of this thread's virtual lane (w = warp, l = lane)
+
+  // global index of scan-order position t of chunk c
+  auto gidx = [&](long long c, long long t) -> long long { return REV ? a.n - 1 - (c * C + t) : c * C + t; };
+  // a chunk is prefetched with 16-byte copies when it is full and its global
+  // range starts on a 16-byte boundary
+  auto can_prefetch = [&](long long c) -> bool {
+    if ((c + 1) * C > a.n) return false;
+    const long long g0 = REV ? a.n - (c + 1) * C : c * C;
+    return (reinterpret_cast<uintptr_t>(a.x + g0) & 15) == 0;
+  };
+  auto prefetch = [&](long long c, int hb) {
+    const long long g0 = REV ? a.n - (c + 1) * C : c * C;
+    const T* src = a.x + g0;
+#pragma unroll
+    for (int q = 0; q < C / PER16 / 1024; ++q) {
+      const int i = tid + 1024 * q;              // 16-byte piece i of the chunk, in address order
+      const int j0 = i * PER16;                  // first element offset in address order
+      // row (virtual lane) of that piece; rows keep address order in smem
+      const int r = REV ? (C - 1 - j0) / E : j0 / E;
+      const int col = REV ? j0 - (C - (r + 1) * E) : j0 - r * E;
+      cp_async16(stage + r * ROW + col, src + j0);
+    }
+    if (SEG) {
+      const unsigned int* hsrc = a.head_bits + (c * C) / 32;
+      for (int i = tid; i < C / 32 / 4; i += 1024) cp_async16(&sm.heads[hb][i * 4], hsrc + i * 4);
+    }
+    cp_async_commit();
+  };
+
+  T x[E];
+  int hb = 0;   // head-bit buffer of the current chunk
+
+  // Launched cooperatively, so every CTA of the grid is resident.  CTA 0
+  // runs the anchor chain; worker CTA i (1 <= i < G) takes chunks
+  // i-1, i-1+(G-1), ... in increasing order.  Every chunk waits only on
+  // smaller chunks, each worker handles its own chunks in order, so the
+  // smallest unfinished chunk can always proceed; and a worker knows its next
+  // chunk in advance, so it can prefetch it without holding a ticket.
+  if (blockIdx.x == 0) {
+    if (w == 0) anchor_chain<T, SEG>(a);
+    return;
+  }
+  const long long stride = gridDim.x - 1;
+  long long c = blockIdx.x - 1;
+  if (c >= a.nchunks) return;
+  bool cur_from_stage = false;
+  if (can_prefetch(c)) {
+    prefetch(c, hb);
+    cur_from_stage = true;
+  }
+  long long pend_pos = -1, pend_chunk = 0;   // deferred first element of an exclusive chunk (thread 0)
+
+  while (true) {
+    // ---- bring chunk c into registers
+    if (cur_from_stage) {
+      cp_async_wait_all();
+      __syncthreads();
+      row_to_regs<T, E, REV>(stage + tid * ROW, x);
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const long long t = (long long)c * C + t0 + e;
+        x[e] = t < a.n ? a.x[gidx(c, t0 + e)] : absent<T>();
+      }
+      if (SEG) {
+        const long long w0 = (c * C) / 32, nwords = (a.n + 31) / 32;
+        for (int i = tid; i < C / 32; i += 1024) sm.heads[hb][i] = (w0 + i < nwords) ? a.head_bits[w0 + i] : 0u;
+      }
+    }
+    if (tid == 0) sm.wtf = 0u;
+    __syncthreads();   // stage consumed, heads visible
+    const long long cn = c + stride;
+    bool next_from_stage = false;
+    if (cn < a.nchunks && can_prefetch(cn)) {
+      prefetch(cn, hb ^ 1);
+      next_from_stage = true;
+    }
+    const unsigned int* heads = sm.heads[hb];
+    auto head = [&](int t) -> bool { return SEG && ((heads[t >> 5] >> (t & 31)) & 1u); };
+    const long long base = c * C;
+    const long long nvalid = min((long long)C, a.n - base);
+
+    // ---- phase 1: lane fold, Kogge-Stone over lanes
+    T acc = x[0];
+    bool f = head(t0);
+#pragma unroll
+    for (int e = 1; e < E; ++e) {
+      bool fr;
+      segop<T, SEG>(f, acc, head(t0 + e), x[e], fr, acc);
+      f = fr;
+    }
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const T o = __shfl_up_sync(0xffffffffu, acc, d);
+      const bool of = __shfl_up_sync(0xffffffffu, (int)f, d);
+      if (lane >= d) {
+        bool fr;
+        segop<T, SEG>(of, o, f, acc, fr, acc);
+        f = fr;
+      }
+    }
+    T lx = __shfl_up_sync(0xffffffffu, acc, 1);
+    bool lxf = __shfl_up_sync(0xffffffffu, (int)f, 1);
+    if (lane == 0) {
+      lx = absent<T>();
+      lxf = false;
+    }
+    if (lane == 31) sm.wt[w] = acc;
+    if (SEG && lane == 31 && f) atomicOr(&sm.wtf, 1u << w);
+    __syncthreads();
+
+    // ---- aggregate, publication, anchored look-back (warp 0)
+    if (w == 0) {
+      T wa = sm.wt[lane];
+      bool wf = SEG && ((sm.wtf >> lane) & 1u);
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const T o = __shfl_up_sync(0xffffffffu, wa, d);
+        const bool of = __shfl_up_sync(0xffffffffu, (int)wf, d);
+        if (lane >= d) {
+          bool fr;
+          segop<T, SEG>(of, o, wf, wa, fr, wa);
+          wf = fr;
+        }
+      }
+      T wx = __shfl_up_sync(0xffffffffu, wa, 1);
+      bool wxf = __shfl_up_sync(0xffffffffu, (int)wf, 1);
+      if (lane == 0) {
+        wx = absent<T>();
+        wxf = false;
+      }
+      sm.wx[lane] = wx;
+      const unsigned int wxm = __ballot_sync(0xffffffffu, wxf);
+      const T agg = __shfl_sync(0xffffffffu, wa, 31);
+      const bool aggf = __shfl_sync(0xffffffffu, (int)wf, 31);
+      if (lane == 0) {
+        sm.wxf = wxm;
+        publish<T>(a.desc + c, agg);
+      }
+      const long long k = c / 32;
+      const int j = (int)(c % 32);
+      T v = absent<T>();
+      bool vf = false;
+      if (lane < j) {
+        const long long q = c - 1 - lane;
+        wait_value<T>(a.desc + q, v, a.status, a.timeout_ns);
+        vf = SEG && a.has_head[q];
+      } else if (lane == j && k > 0) {
+        wait_value<T>(a.anchors + (k - 1), v, a.status, a.timeout_ns);
+        vf = SEG;
+      }
+#pragma unroll
+      for (int s = 1; s < 32; s <<= 1) {
+        const T o = __shfl_xor_sync(0xffffffffu, v, s);
+        const bool of = __shfl_xor_sync(0xffffffffu, (int)vf, s);
+        bool fr;
+        if (lane & s)
+          segop<T, SEG>(vf, v, of, o, fr, v);
+        else
+          segop<T, SEG>(of, o, vf, v, fr, v);
+        vf = fr;
+      }
+      if (lane == 0) {
+        sm.excl = v;
+        sm.exclf = vf;
+      }
+      (void)aggf;
+    }
+    __syncthreads();
+
+    // ---- phase 2: element values (inclusive), in place in x
+    {
+      bool f1, f2;
+      T y;
+      segop<T, SEG>(SEG && sm.exclf, sm.excl, SEG && ((sm.wxf >> w) & 1u), sm.wx[w], f1, y);
+      segop<T, SEG>(f1, y, lxf, lx, f2, y);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        y = (SEG && head(t0 + e)) ? x[e] : y + x[e];
+        x[e] = y;
+      }
+    }
+    if (EXCL && tid == 1023 && c + 1 < a.nchunks) publish<T>(a.tails + c, x[E - 1]);
+    if (a.total_out && base + t0 <= a.n - 1 && a.n - 1 < base + t0 + E) *a.total_out = x[a.n - 1 - base - t0];
+
+    // ---- outputs
+    const bool full = nvalid == C;
+    if (!EXCL) {
+      const long long g0 = REV ? a.n - base - t0 - E : base + t0;
+      if (full && (reinterpret_cast<uintptr_t>(a.y + g0) & 31) == 0) {
+        regs_to_global_256<T, E, REV>(a.y + g0, x);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          if (t0 + e < nvalid) a.y[gidx(c, t0 + e)] = x[e];
+      }
+    } else {
+      // previous inclusive value for this lane's first element
+      if (lane == 31) sm.last[w] = x[E - 1];
+      T pl = __shfl_up_sync(0xffffffffu, x[E - 1], 1);
+      __syncthreads();
+      if (lane == 0) pl = (w > 0) ? sm.last[w - 1] : T(0.0);   // chunk start: written later
+#pragma unroll
+      for (int e = E - 1; e > 0; --e) x[e] = (SEG && head(t0 + e)) ? T(0.0) : x[e - 1];
+      x[0] = (SEG && head(t0)) ? T(0.0) : pl;
+      const long long g0 = REV ? a.n - base - t0 - E : base + t0;
+      if (full && (reinterpret_cast<uintptr_t>(a.y + g0) & 31) == 0) {
+        regs_to_global_256<T, E, REV>(a.y + g0, x);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          if (t0 + e < nvalid) a.y[gidx(c, t0 + e)] = x[e];
+      }
+      if (tid == 0) {
+        // the chunk's first element is the previous chunk's last inclusive
+        // value: resolve the one deferred from the chunk before this one,
+        // then defer this one (its predecessor may still be writing)
+        if (pend_pos >= 0) {
+          T v;
+          wait_value<T>(a.tails + (pend_chunk - 1), v, a.status, a.timeout_ns);
+          a.y[pend_pos] = v;
+        }
+        pend_pos = -1;
+        if (c > 0 && !(SEG && head(0))) {
+          pend_pos = gidx(c, 0);
+          pend_chunk = c;
+        }
+      }
+    }
+
+    if (cn >= a.nchunks) break;
+    c = cn;
+    cur_from_stage = next_from_stage;
+    hb ^= next_from_stage ? 1 : 0;
+    __syncthreads();   // shared arrays of this chunk are no longer read
+  }
+  if (EXCL && tid == 0 && pend_pos >= 0) {
+    T v;
+    wait_value<T>(a.tails + (pend_chunk - 1), v, a.status, a.timeout_ns);
+    a.y[pend_pos] = v;
   }
 }
 
@@ -418,12 +795,35 @@ static ScanWs<T> scan_ws_layout(long long n, bool seg) {
 
 template <typename T, bool SEG, bool REV, bool EXCL>
 static cudaError_t launch_scan(const ScanArgs<T>& a, int threads, cudaStream_t s) {
+  if (threads == 1024) {
+    // persistent: one CTA per SM (cooperative launch), chunks assigned round-robin
+    const size_t smem = ScanGeom<T>::kStageBytes + sizeof(KeepSmem<T>);
+    auto kern = scan_keep_kernel<T, SEG, REV, EXCL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return cudaErrorUnknown;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 1024, smem);
+    if (e != cudaSuccess) return e;
+    const long long grid = min((long long)sms * per_sm, a.nchunks + 1);
+    if (grid >= 2) {
+      void* args[] = {const_cast<ScanArgs<T>*>(&a)};
+      launch_begin(SEG ? "det_segmented_scan" : "det_scan", s);
+      e = cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(1024), args, smem, s);
+      launch_end(s);
+      return e;
+    }
+    // a grid of one CTA cannot hold a worker and the chain: use the
+    // shared-memory kernel below
+  }
   const size_t smem = ScanGeom<T>::kStageBytes + sizeof(ScanSmem<T>);
   auto kern = scan_kernel<T, SEG, REV, EXCL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   launch_begin(SEG ? "det_segmented_scan" : "det_scan", s);
-  kern<<<(unsigned)a.nchunks, threads, smem, s>>>(a);
+  kern<<<(unsigned)(a.nchunks + 1), threads, smem, s>>>(a);
   launch_end(s);
   return cudaGetLastError();
 }
@@ -452,6 +852,7 @@ static int scan_impl(const T* x, T* y, long long n, const long long* seg_off, lo
   a.head_bits = nullptr;
   a.has_head = nullptr;
   a.ticket = &h->ticket;
+  a.role = &h->ticket2;
   a.status = &h->status;
   a.total_out = total_out;
   a.timeout_ns = 2000000000ull;

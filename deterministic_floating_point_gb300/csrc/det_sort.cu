@@ -2,14 +2,14 @@
 // filter, and the segmented pairwise tree over the sorted values.
 //
 //   count p   per tile of K = threads * 32 records: digit counts of the
-//             valid records (warp multi-split by ballots, one shared atomic
-//             per digit group: integer adds, order-free)
+//             valid records (shared integer atomics: order-free)
 //   colscan p per digit: exclusive prefix of the counts over tiles, and the
 //             digit totals (pass 0 also sums them into the valid count)
-//   pass p    per tile, independently: digit starts from the totals, warp
-//             multi-split ranks against per-warp shared counters give each
-//             record its rank among earlier records of its digit inside the
-//             warp; position = digit start + tile prefix + warp prefix + rank.
+//   pass p    per tile, independently: digit starts from the totals; a warp
+//             multi-split (peer masks OR-ed into per-warp shared words) and
+//             per-warp shared counters give each record its rank among
+//             earlier records of its digit inside the warp; position = digit
+//             start + tile prefix + warp prefix + rank.
 //             Records keep their input order inside a digit: the pass is
 //             stable, so after the last pass each destination's records are
 //             in ascending original index.
@@ -25,18 +25,6 @@ namespace {
 
 constexpr int kIPT = 32;                 // records per thread per tile
 // ---------------------------------------------------------------------------
-// Lanes of this warp whose (valid) digit equals mine, by one ballot per
-// digit bit (a warp multi-split); invalid lanes belong to no group.
-__device__ __forceinline__ unsigned digit_peers(unsigned d, bool valid, int D) {
-  unsigned peers = __ballot_sync(0xffffffffu, valid);
-  for (int b = 0; b < D; ++b) {
-    const bool bit = (d >> b) & 1u;
-    const unsigned bb = __ballot_sync(0xffffffffu, bit);
-    peers &= bit ? bb : ~bb;
-  }
-  return peers;
-}
-
 struct PassArgs {
   const int32_t* keys_in;
   const void* vals_in;
@@ -93,9 +81,19 @@ __global__ void __launch_bounds__(1024) sort_count_kernel(PassArgs a) {
     for (int r = 0; r < kIPT; ++r) dg[r] = record_digit<FIRST, false>(a, wbase + (long long)r * 32 + lane, N, mask);
 #pragma unroll
     for (int r = 0; r < kIPT; ++r) {
-      const bool valid = dg[r] != 0xffffffffu;
-      const unsigned peers = digit_peers(dg[r], valid, a.D);
-      if (valid && lane == __ffs(peers) - 1) atomicAdd(&cnt[dg[r]], (unsigned)__popc(peers));
+      // one shared atomic per record, except that the records sharing lane
+      // 0's digit are added by one atomic (a hot digit would otherwise
+      // serialise on one address); integer adds, so the order is free
+      const unsigned d = dg[r];
+      const bool valid = d != 0xffffffffu;
+      const unsigned d0 = __shfl_sync(0xffffffffu, d, 0);
+      const bool in0 = valid && d == d0;
+      const unsigned same0 = __ballot_sync(0xffffffffu, in0);
+      if (in0) {
+        if (lane == __ffs(same0) - 1) atomicAdd(&cnt[d], (unsigned)__popc(same0));
+      } else if (valid) {
+        atomicAdd(&cnt[d], 1u);
+      }
     }
   }
   __syncthreads();
@@ -195,8 +193,9 @@ __global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const int ndig = 1 << a.D;
   const unsigned mask = (unsigned)ndig - 1u;
-  unsigned short* wcnt = reinterpret_cast<unsigned short*>(smem_raw);                          // [nwarps][ndig]
-  unsigned int* gbase = reinterpret_cast<unsigned int*>(smem_raw + (size_t)nwarps * ndig * 2);  // [ndig + 1]
+  unsigned int* pmask = reinterpret_cast<unsigned int*>(smem_raw);                           // [nwarps][ndig]
+  unsigned short* wcnt = reinterpret_cast<unsigned short*>(smem_raw + (size_t)nwarps * ndig * 4); // [nwarps][ndig]
+  unsigned int* gbase = reinterpret_cast<unsigned int*>(smem_raw + (size_t)nwarps * ndig * 6);  // [ndig + 1]
   __shared__ unsigned int wsum[32];
 
   const long long tile = blockIdx.x;
@@ -209,7 +208,10 @@ __global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
   // digit starts (from the column totals) plus this tile's column prefixes
   digit_starts(a.totals, ndig, gbase, wsum);
   for (int d = tid; d < ndig; d += blockDim.x) gbase[d] += a.counts[tile * ndig + d];
-  for (int d = lane; d < ndig; d += 32) wcnt[warp * ndig + d] = 0;
+  for (int d = lane; d < ndig; d += 32) {
+    wcnt[warp * ndig + d] = 0;
+    pmask[warp * ndig + d] = 0u;
+  }
   __syncwarp();
 
   // ---- load this warp's digits (all loads in flight), then rank inside the
@@ -217,15 +219,28 @@ __global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
   unsigned packed[kIPT];
 #pragma unroll
   for (int r = 0; r < kIPT; ++r) packed[r] = record_digit<FIRST, true>(a, wbase + (long long)r * 32 + lane, N, mask);
+  // The lanes of a round that share a digit ("peers") are found without a
+  // warp vote per digit bit: lanes with lane 0's digit by one ballot, the
+  // others by OR-ing their lane bit into a per-warp mask word of their digit
+  // (OR is order-free, so the mask -- and the rank -- are deterministic).
+  unsigned* pm = pmask + warp * ndig;
+  unsigned short* wc = wcnt + warp * ndig;
 #pragma unroll
   for (int r = 0; r < kIPT; ++r) {
-    const bool valid = packed[r] != 0xffffffffu;
     const unsigned d = packed[r];
-    const unsigned peers = digit_peers(d, valid, a.D);
-    unsigned base = 0;
-    if (valid) base = wcnt[warp * ndig + d];
+    const bool valid = d != 0xffffffffu;
+    const unsigned d0 = __shfl_sync(0xffffffffu, d, 0);
+    const bool in0 = valid && d == d0;
+    const unsigned same0 = __ballot_sync(0xffffffffu, in0);
+    if (valid && !in0) atomicOr(pm + d, 1u << lane);
     __syncwarp();
-    if (valid && lane == __ffs(peers) - 1) wcnt[warp * ndig + d] = (unsigned short)(base + __popc(peers));
+    const unsigned peers = in0 ? same0 : (valid ? pm[d] : 0u);
+    const unsigned base = valid ? wc[d] : 0u;
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) {
+      wc[d] = (unsigned short)(base + __popc(peers));
+      if (!in0) pm[d] = 0u;
+    }
     __syncwarp();
     packed[r] = valid ? ((d << 16) | (base + __popc(peers & ((1u << lane) - 1u)))) : 0xffffffffu;
   }
@@ -446,7 +461,7 @@ template <int VB>
 static cudaError_t launch_pass(const PassArgs& a, bool first, bool idx, bool keys_out, int threads, long long tiles,
                                cudaStream_t s) {
   const int ndig = 1 << a.D;
-  const size_t smem = (size_t)(threads / 32) * ndig * 2 + (size_t)(ndig + 1) * 4;
+  const size_t smem = (size_t)(threads / 32) * ndig * 6 + (size_t)(ndig + 1) * 4;
   void (*k)(PassArgs) = nullptr;
 #define DET_PICK(F, I, KO) \
   if (first == F && idx == I && keys_out == KO) k = sort_pass_kernel<VB, F, I, KO>;

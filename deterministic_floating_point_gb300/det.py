@@ -46,6 +46,11 @@ _SIGNATURES = {
     "det_profile_event_count": (_int, []),
     "det_profile_event_name": (ctypes.c_char_p, [_int]),
     "det_launch_count": (ctypes.c_ulonglong, []),
+    "det_atomic_sum": (_int, [_vp, _i64, _int, _vp, _vp]),
+    "det_atomic_scatter_add": (_int, [_vp, _i64, _vp, _vp, _i64, _int, _vp]),
+    "det_atomic_scatter_add_rows": (_int, [_vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _int, _vp]),
+    "det_dlb_scan_workspace_bytes": (_sz, [_i64, _int]),
+    "det_dlb_scan": (_int, [_vp, _vp, _i64, _int, _vp, _sz, _vp]),
 }
 
 
@@ -264,3 +269,34 @@ class KernelTimer:
 
 def launch_count() -> int:
     return int(lib().det_launch_count())
+
+
+# ---------------------------------------------------------------------------
+# nondeterministic baselines (include/det_baselines.h): comparison only
+
+
+def atomic_sum(x: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
+    _check(lib().det_atomic_sum(_ptr(x), x.numel(), _code(x), _ptr(out), _stream(stream)), "det_atomic_sum")
+    return out
+
+
+def atomic_scatter_add(out: torch.Tensor, bins: torch.Tensor, values: torch.Tensor, stream=None) -> torch.Tensor:
+    _check(lib().det_atomic_scatter_add(_ptr(out), out.numel(), _ptr(bins), _ptr(values), values.numel(),
+                                        _code(values), _stream(stream)), "det_atomic_scatter_add")
+    return out
+
+
+def atomic_scatter_add_rows(dst, idx, src, prev_out=None, row_offset: int = 0, stream=None):
+    R, W = dst.shape
+    _check(lib().det_atomic_scatter_add_rows(_ptr(dst), R, W, _ptr(idx), int(row_offset), _ptr(src), src.shape[0],
+                                             _ptr(prev_out), _code(src), _stream(stream)),
+           "det_atomic_scatter_add_rows")
+    return dst
+
+
+def dlb_scan(x: torch.Tensor, y: torch.Tensor, workspace: torch.Tensor | None = None, stream=None):
+    nbytes = lib().det_dlb_scan_workspace_bytes(x.numel(), _code(x))
+    ws = _ws(workspace, nbytes, x.device)
+    _check(lib().det_dlb_scan(_ptr(x), _ptr(y), x.numel(), _code(x), _ptr(ws), ws.numel(), _stream(stream)),
+           "det_dlb_scan")
+    return y
