@@ -69,19 +69,25 @@ def _timed_oracle(fn, budget_s=3.0):
 
 
 def fingerprint(torch, *tensors):
-    """Exact fingerprint of result bits: SHA-256 of small results, a
-    position-weighted 64-bit integer sum of the bit patterns for large ones."""
+    """Fingerprint of result bits: SHA-256 of small results; for large ones,
+    SHA-256 of per-block weighted sums of the bit patterns (integer
+    arithmetic, so any changed element changes some block sum)."""
     import hashlib as _h
     hs = _h.sha256()
     for t in tensors:
         nbytes = t.numel() * t.element_size()
         if nbytes <= (64 << 20):
             hs.update(t.detach().cpu().numpy().tobytes())
-        else:
-            bits = t.view(torch.int64 if t.element_size() == 8 else torch.int32).to(torch.int64)
-            g = torch.Generator(device=t.device).manual_seed(12345)
-            mult = torch.randint(1, 1 << 62, (bits.numel(),), generator=g, device=t.device, dtype=torch.int64) | 1
-            hs.update(str(int((bits.flatten() * mult).sum().item())).encode())
+            continue
+        bits = t.detach().reshape(-1).view(torch.int64 if t.element_size() == 8 else torch.int32)
+        k = 8192
+        pad = (-bits.numel()) % k
+        if pad:
+            bits = torch.cat([bits, bits.new_zeros(pad)])
+        blocks = bits.view(-1, k)
+        w = torch.arange(1, 2 * k, 2, device=t.device, dtype=bits.dtype)
+        hs.update(blocks.sum(dim=1, dtype=torch.int64).cpu().numpy().tobytes())
+        hs.update((blocks * w).sum(dim=1, dtype=torch.int64).cpu().numpy().tobytes())
     return hs.hexdigest()
 
 

@@ -159,7 +159,8 @@ __global__ void __launch_bounds__(kDlbThreads) dlb_scan_kernel(const T* __restri
       }
       const unsigned im = __ballot_sync(0xffffffffu, isinc);
       const int f = __ffs(im) - 1;            // nearest inclusive predecessor in this window
-      T part = lane <= f ? val : T(0);
+      const int last = f < 0 ? 31 : f;        // no inclusive one: the whole window is partial
+      T part = lane <= last ? val : T(0);
 #pragma unroll
       for (int s = 16; s > 0; s >>= 1) part += __shfl_xor_sync(0xffffffffu, part, s);
       run += part;

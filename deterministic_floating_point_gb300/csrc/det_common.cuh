@@ -100,6 +100,51 @@ __device__ __forceinline__ T warp_pt(T v) {
   return v;
 }
 
+// Binary counter of pairwise-tree nodes.  push() takes the nodes of
+// consecutive aligned blocks (all of one level) in order and merges equal
+// levels as a binary counter does: the new node is added to the pending node
+// of each lower level it completes, the earlier node always the left operand.
+// result() folds the pending nodes from the smallest upwards, which is the
+// pairwise tree over all blocks with absent padding.  Levels below L live in
+// registers and are indexed only statically; deeper levels (more than 2^L
+// blocks) use a small local array.
+template <typename T, int L>
+struct NodeCounter {
+  T st[L];
+  T deep[40 - L];
+  unsigned long long cnt = 0;
+
+  __device__ __forceinline__ void push(T node) {
+    const int z = __ffsll((long long)~cnt) - 1;   // levels completed by this node
+#pragma unroll
+    for (int l = 0; l < L; ++l)
+      if (l < z) node = st[l] + node;
+    for (int l = L; l < z; ++l) node = deep[l - L] + node;
+#pragma unroll
+    for (int l = 0; l < L; ++l)
+      if (l == z) st[l] = node;
+    if (z >= L) deep[z - L] = node;
+    ++cnt;
+  }
+
+  __device__ __forceinline__ T result() const {
+    T res = absent<T>();
+    bool have = false;
+#pragma unroll
+    for (int l = 0; l < L; ++l)
+      if ((cnt >> l) & 1ull) {
+        res = have ? st[l] + res : st[l];
+        have = true;
+      }
+    for (int l = L; l < 40; ++l)
+      if ((cnt >> l) & 1ull) {
+        res = have ? deep[l - L] + res : deep[l - L];
+        have = true;
+      }
+    return res;
+  }
+};
+
 // ---------------------------------------------------------------------------
 // Memory-model helpers for flags and published values.
 __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {

@@ -40,8 +40,7 @@ rows_kernel(T* __restrict__ dst, long long R, long long W, const T* __restrict__
       col[c] = c0 + c * 32 + lane;
       cok[c] = col[c] < W;
     }
-    T stack[kCPL][40];
-    long long cnt = 0;
+    NodeCounter<T, 8> nc[kCPL];
     for (long long k0 = 0; k0 < L; k0 += 8) {
       T v[kCPL][8];
 #pragma unroll
@@ -52,33 +51,12 @@ rows_kernel(T* __restrict__ dst, long long R, long long W, const T* __restrict__
 #pragma unroll
         for (int c = 0; c < kCPL; ++c) v[c][e] = (in && cok[c]) ? __ldg(src + s * W + col[c]) : absent<T>();
       }
-      T node[kCPL];
 #pragma unroll
-      for (int c = 0; c < kCPL; ++c) node[c] = thread_pt(v[c]);   // 8 rows -> level-3 node
-      int lvl = 0;
-      long long q = cnt;
-      while (q & 1) {
-#pragma unroll
-        for (int c = 0; c < kCPL; ++c) node[c] = stack[c][lvl] + node[c];
-        q >>= 1;
-        ++lvl;
-      }
-#pragma unroll
-      for (int c = 0; c < kCPL; ++c) stack[c][lvl] = node[c];
-      ++cnt;
+      for (int c = 0; c < kCPL; ++c) nc[c].push(thread_pt(v[c]));   // 8 rows -> level-3 node
     }
     T tree[kCPL];
 #pragma unroll
-    for (int c = 0; c < kCPL; ++c) {
-      bool have = false;
-      tree[c] = absent<T>();
-      for (int lvl = 0; lvl < 40; ++lvl) {
-        if ((cnt >> lvl) & 1) {
-          tree[c] = have ? stack[c][lvl] + tree[c] : stack[c][lvl];
-          have = true;
-        }
-      }
-    }
+    for (int c = 0; c < kCPL; ++c) tree[c] = nc[c].result();
     T old[kCPL];
 #pragma unroll
     for (int c = 0; c < kCPL; ++c) old[c] = cok[c] ? dst[r * W + col[c]] : T(0);

@@ -513,13 +513,15 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
     const long long g0 = REV ? a.n - (c + 1) * C : c * C;
     return (reinterpret_cast<uintptr_t>(a.x + g0) & 15) == 0;
   };
-  auto prefetch = [&](long long c, int hb) {
+  // Issue the copies of chunk c into the stage, spread over threads
+  // [first, 1024) of the CTA.
+  auto prefetch = [&](long long c, int hb, int first) {
     const long long g0 = REV ? a.n - (c + 1) * C : c * C;
     const T* src = a.x + g0;
-#pragma unroll
-    for (int q = 0; q < C / PER16 / 1024; ++q) {
-      const int i = tid + 1024 * q;              // 16-byte piece i of the chunk, in address order
-      const int j0 = i * PER16;                  // first element offset in address order
+    const int nthr = 1024 - first, me = tid - first;
+    if (me < 0) return;
+    for (int i = me; i < C / PER16; i += nthr) {
+      const int j0 = i * PER16;                  // first element offset of 16-byte piece i, address order
       // row (virtual lane) of that piece; rows keep address order in smem
       const int r = REV ? (C - 1 - j0) / E : j0 / E;
       const int col = REV ? j0 - (C - (r + 1) * E) : j0 - r * E;
@@ -527,7 +529,7 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
     }
     if (SEG) {
       const unsigned int* hsrc = a.head_bits + (c * C) / 32;
-      for (int i = tid; i < C / 32 / 4; i += 1024) cp_async16(&sm.heads[hb][i * 4], hsrc + i * 4);
+      for (int i = me; i < C / 32 / 4; i += nthr) cp_async16(&sm.heads[hb][i * 4], hsrc + i * 4);
     }
     cp_async_commit();
   };
@@ -550,7 +552,7 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
   if (c >= a.nchunks) return;
   bool cur_from_stage = false;
   if (can_prefetch(c)) {
-    prefetch(c, hb);
+    prefetch(c, hb, 0);
     cur_from_stage = true;
   }
   long long pend_pos = -1, pend_chunk = 0;   // deferred first element of an exclusive chunk (thread 0)
@@ -575,11 +577,7 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
     if (tid == 0) sm.wtf = 0u;
     __syncthreads();   // stage consumed, heads visible
     const long long cn = c + stride;
-    bool next_from_stage = false;
-    if (cn < a.nchunks && can_prefetch(cn)) {
-      prefetch(cn, hb ^ 1);
-      next_from_stage = true;
-    }
+    const bool next_from_stage = cn < a.nchunks && can_prefetch(cn);
     const unsigned int* heads = sm.heads[hb];
     auto head = [&](int t) -> bool { return SEG && ((heads[t >> 5] >> (t & 31)) & 1u); };
     const long long base = c * C;
@@ -614,7 +612,9 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
     if (SEG && lane == 31 && f) atomicOr(&sm.wtf, 1u << w);
     __syncthreads();
 
-    // ---- aggregate, publication, anchored look-back (warp 0)
+    // ---- aggregate, publication, anchored look-back (warp 0); meanwhile
+    // warps 1..31 issue the copies of the next chunk into the free stage
+    if (w != 0 && next_from_stage) prefetch(cn, hb ^ 1, 32);
     if (w == 0) {
       T wa = sm.wt[lane];
       bool wf = SEG && ((sm.wtf >> lane) & 1u);
@@ -686,7 +686,15 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
       }
     }
     if (EXCL && tid == 1023 && c + 1 < a.nchunks) publish<T>(a.tails + c, x[E - 1]);
-    if (a.total_out && base + t0 <= a.n - 1 && a.n - 1 < base + t0 + E) *a.total_out = x[a.n - 1 - base - t0];
+    if (a.total_out && base + t0 <= a.n - 1 && a.n - 1 < base + t0 + E) {
+      // static indices only: a dynamic index would move x[] to local memory
+      const long long want = a.n - 1 - base - t0;
+      T tv = x[0];
+#pragma unroll
+      for (int e = 1; e < E; ++e)
+        if (e == want) tv = x[e];
+      *a.total_out = tv;
+    }
 
     // ---- outputs
     const bool full = nvalid == C;

@@ -38,6 +38,7 @@ struct PassArgs {
   int shift;
   int D;
   long long tiles;
+  long long K;                 // records per tile
   unsigned int* counts;        // [tiles][ndig]: tile counts, then exclusive column prefixes
   unsigned int* totals;        // [ndig] column totals
   unsigned int* status;
@@ -59,41 +60,68 @@ __device__ __forceinline__ unsigned record_digit(const PassArgs& a, long long i,
   return ((unsigned)raw >> a.shift) & mask;
 }
 
-// counts[tile][d] = records of the tile with digit d.  Same tiling as the
-// scatter pass: K = blockDim.x * kIPT records, warp w owns a contiguous
-// 32 * kIPT slice.
+// counts[tile][d] = records of the tile with digit d.  The tile is the
+// scatter pass's tile (K = pass_threads * kIPT records); counting is
+// order-free, so here each thread simply streams its share of the tile with
+// 16-byte loads, several in flight, and adds one shared atomic per record
+// (records sharing lane 0's digit are added by one atomic, so a hot digit
+// does not serialise on one address).
 template <bool FIRST>
-__global__ void __launch_bounds__(1024) sort_count_kernel(PassArgs a) {
+__global__ void __launch_bounds__(256) sort_count_kernel(PassArgs a, long long K) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned int* cnt = reinterpret_cast<unsigned int*>(smem_raw);   // [ndig]
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int ndig = 1 << a.D;
   const unsigned mask = (unsigned)ndig - 1u;
   const long long tile = blockIdx.x;
   const long long N = FIRST ? a.n : (long long)*a.n_valid;
   for (int d = tid; d < ndig; d += blockDim.x) cnt[d] = 0u;
   __syncthreads();
-  const long long K = (long long)blockDim.x * kIPT;
-  const long long wbase = tile * K + (long long)warp * 32 * kIPT;
-  if (tile * K < N) {
-    unsigned dg[kIPT];
-#pragma unroll
-    for (int r = 0; r < kIPT; ++r) dg[r] = record_digit<FIRST, false>(a, wbase + (long long)r * 32 + lane, N, mask);
-#pragma unroll
-    for (int r = 0; r < kIPT; ++r) {
-      // one shared atomic per record, except that the records sharing lane
-      // 0's digit are added by one atomic (a hot digit would otherwise
-      // serialise on one address); integer adds, so the order is free
-      const unsigned d = dg[r];
-      const bool valid = d != 0xffffffffu;
-      const unsigned d0 = __shfl_sync(0xffffffffu, d, 0);
-      const bool in0 = valid && d == d0;
-      const unsigned same0 = __ballot_sync(0xffffffffu, in0);
-      if (in0) {
-        if (lane == __ffs(same0) - 1) atomicAdd(&cnt[d], (unsigned)__popc(same0));
-      } else if (valid) {
-        atomicAdd(&cnt[d], 1u);
+  const long long t0 = tile * K, t1 = min(N, t0 + K);
+  auto count = [&](int k, bool in) {
+    unsigned d = 0xffffffffu;
+    if (in) {
+      if (FIRST) {
+        const long long kk = (long long)k + a.key_offset;
+        if (kk >= 0 && kk < a.m) d = ((unsigned)kk >> a.shift) & mask;
+      } else {
+        d = ((unsigned)k >> a.shift) & mask;
       }
+    }
+    const bool valid = d != 0xffffffffu;
+    const unsigned d0 = __shfl_sync(0xffffffffu, d, 0);
+    const bool in0 = valid && d == d0;
+    const unsigned same0 = __ballot_sync(0xffffffffu, in0);
+    if (in0) {
+      if (lane == __ffs(same0) - 1) atomicAdd(&cnt[d], (unsigned)__popc(same0));
+    } else if (valid) {
+      atomicAdd(&cnt[d], 1u);
+    }
+  };
+  if (t0 < t1) {
+    const bool vec = (reinterpret_cast<uintptr_t>(a.keys_in + t0) & 15) == 0;
+    constexpr int U = 4;   // 16-byte loads in flight per thread per step
+    long long i = t0;
+    if (vec) {
+      const long long span = (long long)blockDim.x * 4 * U;
+      for (; i + span <= t1; i += span) {
+        int4 q[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          q[u] = __ldg(reinterpret_cast<const int4*>(a.keys_in + i + (long long)u * blockDim.x * 4) + tid);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          count(q[u].x, true);
+          count(q[u].y, true);
+          count(q[u].z, true);
+          count(q[u].w, true);
+        }
+      }
+    }
+    // remainder: whole warps step together, lanes past the end count nothing
+    for (long long b = i + (long long)(tid & ~31); b < t1; b += blockDim.x) {
+      const long long j = b + lane;
+      count(j < t1 ? __ldg(a.keys_in + j) : 0, j < t1);
     }
   }
   __syncthreads();
@@ -186,7 +214,18 @@ template <> struct Payload<0> { using U = unsigned int; };
 template <> struct Payload<4> { using U = unsigned int; };
 template <> struct Payload<8> { using U = unsigned long long; };
 
-template <int VB, bool FIRST, bool IDX, bool KEYS_OUT>
+// Shared bytes of the staging area of a pass (records in tile-sorted order).
+__host__ __device__ inline size_t pass_staging_bytes(long long K, int vb, bool idx, bool keys_out) {
+  return (size_t)K * (vb + (idx ? 4 : 0) + (keys_out ? 4 : 0) + 2);
+}
+__host__ __device__ inline size_t pass_front_bytes(int nwarps, int ndig, long long K, int vb, bool idx, bool keys_out,
+                                                   bool stage) {
+  const size_t ranking = (size_t)nwarps * ndig * 6;
+  const size_t staging = stage ? pass_staging_bytes(K, vb, idx, keys_out) : 0;
+  return align_up(ranking > staging ? ranking : staging, 16);
+}
+
+template <int VB, bool FIRST, bool IDX, bool KEYS_OUT, bool STAGE>
 __global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
   using U = typename Payload<VB>::U;
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -195,7 +234,8 @@ __global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
   const unsigned mask = (unsigned)ndig - 1u;
   unsigned int* pmask = reinterpret_cast<unsigned int*>(smem_raw);                           // [nwarps][ndig]
   unsigned short* wcnt = reinterpret_cast<unsigned short*>(smem_raw + (size_t)nwarps * ndig * 4); // [nwarps][ndig]
-  unsigned int* gbase = reinterpret_cast<unsigned int*>(smem_raw + (size_t)nwarps * ndig * 6);  // [ndig + 1]
+  unsigned int* gbase = reinterpret_cast<unsigned int*>(
+      smem_raw + pass_front_bytes(nwarps, ndig, a.K, VB, IDX, KEYS_OUT, STAGE));   // [ndig + 1]
   __shared__ unsigned int wsum[32];
 
   const long long tile = blockIdx.x;
@@ -246,7 +286,59 @@ __global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
   }
   __syncthreads();
 
-  // ---- per digit: exclusive prefix over the warps of this tile
+  if (!STAGE) {
+    // ---- direct scatter (payloads too large to stage): warp prefixes, then
+    // each record goes straight to its global position
+    for (int d = tid; d < ndig; d += blockDim.x) {
+      unsigned run = 0;
+      for (int w = 0; w < nwarps; ++w) {
+        const unsigned c = wcnt[w * ndig + d];
+        wcnt[w * ndig + d] = (unsigned short)run;
+        run += c;
+      }
+    }
+    __syncthreads();
+    const U* __restrict__ vin = reinterpret_cast<const U*>(a.vals_in);
+    U* __restrict__ vout = reinterpret_cast<U*>(a.vals_out);
+    const int32_t* __restrict__ iin = a.idx_in;
+    int32_t* __restrict__ iout = a.idx_out;
+    const int32_t* __restrict__ kin = a.keys_in;
+    int32_t* __restrict__ kout = a.keys_out;
+    const unsigned short* __restrict__ wc_tile = wcnt + warp * ndig;
+    constexpr int B = 4;
+#pragma unroll
+    for (int r0 = 0; r0 < kIPT; r0 += B) {
+      U vv[B];
+      int32_t ii[B], kk[B];
+#pragma unroll
+      for (int e = 0; e < B; ++e) {
+        const long long i = wbase + (long long)(r0 + e) * 32 + lane;
+        const bool ok = packed[r0 + e] != 0xffffffffu;
+        if (VB) vv[e] = ok ? __ldg(vin + i) : U(0);
+        if (IDX) ii[e] = ok ? (FIRST ? (int32_t)i : __ldg(iin + i)) : 0;
+        if (KEYS_OUT) kk[e] = ok ? (FIRST ? (int32_t)((long long)__ldg(kin + i) + a.key_offset) : __ldg(kin + i)) : 0;
+      }
+#pragma unroll
+      for (int e = 0; e < B; ++e) {
+        const unsigned pk = packed[r0 + e];
+        if (pk == 0xffffffffu) continue;
+        const unsigned d = pk >> 16;
+        const long long pos = (long long)gbase[d] + wc_tile[d] + (pk & 0xffffu);
+        if (pos < 0 || pos >= a.n) {
+          set_status(a.status, DET_ERR_INVALID_ARG);
+          continue;
+        }
+        if (VB) vout[pos] = vv[e];
+        if (IDX) iout[pos] = ii[e];
+        if (KEYS_OUT) kout[pos] = kk[e];
+      }
+    }
+    return;
+  }
+
+  // ---- per digit: exclusive prefix over the warps of this tile, and the
+  // tile's digit counts
+  unsigned int* lstart = gbase + (ndig + 1);   // [ndig + 1] tile-local digit starts
   for (int d = tid; d < ndig; d += blockDim.x) {
     unsigned run = 0;
     for (int w = 0; w < nwarps; ++w) {
@@ -254,26 +346,77 @@ __global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
       wcnt[w * ndig + d] = (unsigned short)run;
       run += c;
     }
+    lstart[d] = run;   // count for now; turned into starts below
   }
   __syncthreads();
-
-  // ---- move the payload to its sorted position
-  const U* vin = reinterpret_cast<const U*>(a.vals_in);
-  U* vout = reinterpret_cast<U*>(a.vals_out);
+  {
+    // exclusive scan of the tile's digit counts (reuses the digit-start scan)
+    unsigned int* tmp = gbase + 2 * (ndig + 1);   // [ndig + 1]
+    digit_starts(lstart, ndig, tmp, wsum);
+    for (int d = tid; d <= ndig; d += blockDim.x) lstart[d] = tmp[d];
+  }
+  __syncthreads();
+  // tile-local sorted position of each record (digit-major, stable)
 #pragma unroll
   for (int r = 0; r < kIPT; ++r) {
     const unsigned pk = packed[r];
     if (pk == 0xffffffffu) continue;
-    const long long i = wbase + (long long)r * 32 + lane;
     const unsigned d = pk >> 16;
-    const long long pos = (long long)gbase[d] + wcnt[warp * ndig + d] + (pk & 0xffffu);
+    packed[r] = (d << 16) | (lstart[d] + wcnt[warp * ndig + d] + (pk & 0xffffu));
+  }
+  __syncthreads();   // the peer-mask and counter words are free from here on
+
+  // ---- stage the records in shared memory in tile-sorted order, then write
+  // each digit's run to its global place with consecutive threads on
+  // consecutive positions (coalesced runs instead of one sector per record)
+  const long long nvalid_tile = lstart[ndig];
+  unsigned char* stage = smem_raw;   // overlaps pmask / wcnt
+  U* s_val = reinterpret_cast<U*>(stage);
+  int32_t* s_idx = reinterpret_cast<int32_t*>(stage + (size_t)VB * a.K);
+  int32_t* s_key = reinterpret_cast<int32_t*>(stage + (size_t)(VB + (IDX ? 4 : 0)) * a.K);
+  unsigned short* s_dig =
+      reinterpret_cast<unsigned short*>(stage + (size_t)(VB + (IDX ? 4 : 0) + (KEYS_OUT ? 4 : 0)) * a.K);
+  const U* __restrict__ vin = reinterpret_cast<const U*>(a.vals_in);
+  U* __restrict__ vout = reinterpret_cast<U*>(a.vals_out);
+  const int32_t* __restrict__ iin = a.idx_in;
+  int32_t* __restrict__ iout = a.idx_out;
+  const int32_t* __restrict__ kin = a.keys_in;
+  int32_t* __restrict__ kout = a.keys_out;
+  constexpr int B = 4;
+#pragma unroll
+  for (int r0 = 0; r0 < kIPT; r0 += B) {
+    U vv[B];
+    int32_t ii[B], kk[B];
+#pragma unroll
+    for (int e = 0; e < B; ++e) {
+      const long long i = wbase + (long long)(r0 + e) * 32 + lane;
+      const bool ok = packed[r0 + e] != 0xffffffffu;
+      if (VB) vv[e] = ok ? __ldg(vin + i) : U(0);
+      if (IDX) ii[e] = ok ? (FIRST ? (int32_t)i : __ldg(iin + i)) : 0;
+      if (KEYS_OUT) kk[e] = ok ? (FIRST ? (int32_t)((long long)__ldg(kin + i) + a.key_offset) : __ldg(kin + i)) : 0;
+    }
+#pragma unroll
+    for (int e = 0; e < B; ++e) {
+      const unsigned pk = packed[r0 + e];
+      if (pk == 0xffffffffu) continue;
+      const unsigned lp = pk & 0xffffu;
+      if (VB) s_val[lp] = vv[e];
+      if (IDX) s_idx[lp] = ii[e];
+      if (KEYS_OUT) s_key[lp] = kk[e];
+      s_dig[lp] = (unsigned short)(pk >> 16);
+    }
+  }
+  __syncthreads();
+  for (long long i = tid; i < nvalid_tile; i += blockDim.x) {
+    const unsigned d = s_dig[i];
+    const long long pos = (long long)gbase[d] + (i - (long long)lstart[d]);
     if (pos < 0 || pos >= a.n) {   // cannot happen for a correct ranking; never write out of bounds
       set_status(a.status, DET_ERR_INVALID_ARG);
       continue;
     }
-    if (VB) vout[pos] = vin[i];
-    if (IDX) a.idx_out[pos] = FIRST ? (int32_t)i : a.idx_in[i];
-    if (KEYS_OUT) a.keys_out[pos] = FIRST ? (int32_t)((long long)a.keys_in[i] + a.key_offset) : a.keys_in[i];
+    if (VB) vout[pos] = s_val[i];
+    if (IDX) iout[pos] = s_idx[i];
+    if (KEYS_OUT) kout[pos] = s_key[i];
   }
 }
 
@@ -305,34 +448,16 @@ __global__ void sort_bounds_kernel(const int32_t* __restrict__ keys, const unsig
 template <typename T>
 __device__ T warp_pt_range(const T* __restrict__ p, long long len) {
   const int lane = threadIdx.x & 31;
-  T stack[40];
-  long long cnt = 0;
+  NodeCounter<T, 8> nc;
   const long long rounds = (len + 255) / 256;
   for (long long r = 0; r < rounds; ++r) {
     T v[8];
     const long long b = r * 256 + lane * 8;
 #pragma unroll
     for (int e = 0; e < 8; ++e) v[e] = (b + e < len) ? __ldg(p + b + e) : absent<T>();
-    T node = warp_pt(thread_pt(v));
-    int lvl = 0;
-    long long c = cnt;
-    while (c & 1) {
-      node = stack[lvl] + node;
-      c >>= 1;
-      ++lvl;
-    }
-    stack[lvl] = node;
-    ++cnt;
+    nc.push(warp_pt(thread_pt(v)));   // node of the aligned 256-block r (level 8)
   }
-  T res = absent<T>();
-  bool have = false;
-  for (int lvl = 0; lvl < 40; ++lvl) {
-    if ((cnt >> lvl) & 1) {
-      res = have ? stack[lvl] + res : stack[lvl];
-      have = true;
-    }
-  }
-  return res;
+  return nc.result();
 }
 
 struct LongSeg {
@@ -418,7 +543,7 @@ SortPlan make_sort_plan(long long n, long long m, int value_bytes, bool need_idx
   while ((1LL << B) < m) ++B;
   p.passes = B <= 10 ? 1 : (B + 9) / 10;
   p.digit_bits = B == 0 ? 1 : (B + p.passes - 1) / p.passes;
-  p.threads = block_threads ? block_threads : 512;
+  p.threads = block_threads ? block_threads : 256;
   p.ipt = kIPT;
   const long long K = (long long)p.threads * kIPT;
   p.tiles = (n + K - 1) / K;
@@ -461,10 +586,16 @@ template <int VB>
 static cudaError_t launch_pass(const PassArgs& a, bool first, bool idx, bool keys_out, int threads, long long tiles,
                                cudaStream_t s) {
   const int ndig = 1 << a.D;
-  const size_t smem = (size_t)(threads / 32) * ndig * 6 + (size_t)(ndig + 1) * 4;
+  int dev = 0, max_smem = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  const size_t tail = (size_t)3 * (ndig + 1) * 4;
+  const bool stage = pass_front_bytes(threads / 32, ndig, a.K, VB, idx, keys_out, true) + tail <= (size_t)max_smem;
+  const size_t smem = pass_front_bytes(threads / 32, ndig, a.K, VB, idx, keys_out, stage) + tail;
   void (*k)(PassArgs) = nullptr;
-#define DET_PICK(F, I, KO) \
-  if (first == F && idx == I && keys_out == KO) k = sort_pass_kernel<VB, F, I, KO>;
+#define DET_PICK(F, I, KO)                                                            \
+  if (first == F && idx == I && keys_out == KO)                                       \
+    k = stage ? sort_pass_kernel<VB, F, I, KO, true> : sort_pass_kernel<VB, F, I, KO, false>;
   DET_PICK(true, true, true) DET_PICK(true, true, false) DET_PICK(true, false, true) DET_PICK(true, false, false)
   DET_PICK(false, true, true) DET_PICK(false, true, false) DET_PICK(false, false, true) DET_PICK(false, false, false)
 #undef DET_PICK
@@ -506,16 +637,18 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
     a.shift = pass * p.digit_bits;
     a.D = p.digit_bits;
     a.tiles = p.tiles;
+    a.K = (long long)p.threads * kIPT;
     a.counts = counts;
     a.totals = totals;
     a.status = &h->status;
     a.n_valid = &h->n_valid;
     const size_t csmem = (size_t)ndig * 4;
+    const long long K = (long long)p.threads * kIPT;
     launch_begin("det_sort_count", s);
     if (first)
-      sort_count_kernel<true><<<(unsigned)p.tiles, p.threads, csmem, s>>>(a);
+      sort_count_kernel<true><<<(unsigned)p.tiles, 256, csmem, s>>>(a, K);
     else
-      sort_count_kernel<false><<<(unsigned)p.tiles, p.threads, csmem, s>>>(a);
+      sort_count_kernel<false><<<(unsigned)p.tiles, 256, csmem, s>>>(a, K);
     launch_end(s);
     launch_begin("det_sort_colscan", s);
     sort_colscan_kernel<<<(unsigned)((ndig + 31) / 32), 1024, 0, s>>>(a, first ? 1 : 0);
