@@ -485,15 +485,20 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 template <typename T> struct KeepSmem {
   T wt[32];
-  T wx[32];
+  T wx[2][32];            // warp prefixes of the current / next chunk (by parity)
   T last[32];
-  unsigned int wtf, wxf;
+  unsigned int wtf;
+  unsigned int wxf[2];
   T excl;
   int exclf;
-  long long next;
   alignas(16) unsigned int heads[2][ScanGeom<T>::C / 32];   // cp.async destinations: 16-byte aligned
 };
 
+// Software-pipelined by one chunk: in iteration i a CTA runs phase 1 of its
+// next chunk (from the stage) and publishes that chunk's aggregate before it
+// waits in the look-back of its current chunk, so every aggregate -- and the
+// anchor chain built on them -- is published about one round before anyone
+// needs it.
 template <typename T, bool SEG, bool REV, bool EXCL>
 __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
   using G = ScanGeom<T>;
@@ -504,25 +509,20 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int t0 = tid * E;   // first element of this thread's virtual lane (w = warp, l = lane)
 
-  // global index of scan-order position t of chunk c
   auto gidx = [&](long long c, long long t) -> long long { return REV ? a.n - 1 - (c * C + t) : c * C + t; };
-  // a chunk is prefetched with 16-byte copies when it is full and its global
-  // range starts on a 16-byte boundary
   auto can_prefetch = [&](long long c) -> bool {
     if ((c + 1) * C > a.n) return false;
     const long long g0 = REV ? a.n - (c + 1) * C : c * C;
     return (reinterpret_cast<uintptr_t>(a.x + g0) & 15) == 0;
   };
-  // Issue the copies of chunk c into the stage, spread over threads
-  // [first, 1024) of the CTA.
+  // copies of chunk c (and its head bits) into the stage, by threads [first, 1024)
   auto prefetch = [&](long long c, int hb, int first) {
     const long long g0 = REV ? a.n - (c + 1) * C : c * C;
     const T* src = a.x + g0;
     const int nthr = 1024 - first, me = tid - first;
     if (me < 0) return;
     for (int i = me; i < C / PER16; i += nthr) {
-      const int j0 = i * PER16;                  // first element offset of 16-byte piece i, address order
-      // row (virtual lane) of that piece; rows keep address order in smem
+      const int j0 = i * PER16;
       const int r = REV ? (C - 1 - j0) / E : j0 / E;
       const int col = REV ? j0 - (C - (r + 1) * E) : j0 - r * E;
       cp_async16(stage + r * ROW + col, src + j0);
@@ -533,65 +533,18 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
     }
     cp_async_commit();
   };
+  // head bits of a chunk loaded directly (chunks that are not prefetched)
+  auto load_heads = [&](long long c, int hb) {
+    if (!SEG) return;
+    const long long w0 = (c * C) / 32, nwords = (a.n + 31) / 32;
+    for (int i = tid; i < C / 32; i += 1024) sm.heads[hb][i] = (w0 + i < nwords) ? a.head_bits[w0 + i] : 0u;
+  };
+  auto head_of = [&](int hb, int t) -> bool { return SEG && ((sm.heads[hb][t >> 5] >> (t & 31)) & 1u); };
 
-  T x[E];
-  int hb = 0;   // head-bit buffer of the current chunk
-
-  // Launched cooperatively, so every CTA of the grid is resident.  CTA 0
-  // runs the anchor chain; worker CTA i (1 <= i < G) takes chunks
-  // i-1, i-1+(G-1), ... in increasing order.  Every chunk waits only on
-  // smaller chunks, each worker handles its own chunks in order, so the
-  // smallest unfinished chunk can always proceed; and a worker knows its next
-  // chunk in advance, so it can prefetch it without holding a ticket.
-  if (blockIdx.x == 0) {
-    if (w == 0) anchor_chain<T, SEG>(a);
-    return;
-  }
-  const long long stride = gridDim.x - 1;
-  long long c = blockIdx.x - 1;
-  if (c >= a.nchunks) return;
-  bool cur_from_stage = false;
-  if (can_prefetch(c)) {
-    prefetch(c, hb, 0);
-    cur_from_stage = true;
-  }
-  long long pend_pos = -1, pend_chunk = 0;   // deferred first element of an exclusive chunk (thread 0)
-
-  while (true) {
-    // ---- bring chunk c into registers
-    if (cur_from_stage) {
-      cp_async_wait_all();
-      __syncthreads();
-      row_to_regs<T, E, REV>(stage + tid * ROW, x);
-    } else {
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const long long t = (long long)c * C + t0 + e;
-        x[e] = t < a.n ? a.x[gidx(c, t0 + e)] : absent<T>();
-      }
-      if (SEG) {
-        const long long w0 = (c * C) / 32, nwords = (a.n + 31) / 32;
-        for (int i = tid; i < C / 32; i += 1024) sm.heads[hb][i] = (w0 + i < nwords) ? a.head_bits[w0 + i] : 0u;
-      }
-    }
-    if (tid == 0) sm.wtf = 0u;
-    __syncthreads();   // stage consumed, heads visible
-    const long long cn = c + stride;
-    const bool next_from_stage = cn < a.nchunks && can_prefetch(cn);
-    const unsigned int* heads = sm.heads[hb];
-    auto head = [&](int t) -> bool { return SEG && ((heads[t >> 5] >> (t & 31)) & 1u); };
-    const long long base = c * C;
-    const long long nvalid = min((long long)C, a.n - base);
-
-    // ---- phase 1: lane fold, Kogge-Stone over lanes
-    T acc = x[0];
-    bool f = head(t0);
-#pragma unroll
-    for (int e = 1; e < E; ++e) {
-      bool fr;
-      segop<T, SEG>(f, acc, head(t0 + e), x[e], fr, acc);
-      f = fr;
-    }
+  // Phase 1 after the lane fold: Kogge-Stone over lanes (-> lx), then over
+  // warps by warp 0 (-> wx[set]) and publication of Agg(c).  Ends with the
+  // warp prefixes in shared memory once the caller synchronises.
+  auto finish_phase1 = [&](T acc, bool f, int set, long long c, T& lx, bool& lxf) {
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const T o = __shfl_up_sync(0xffffffffu, acc, d);
@@ -602,8 +555,8 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
         f = fr;
       }
     }
-    T lx = __shfl_up_sync(0xffffffffu, acc, 1);
-    bool lxf = __shfl_up_sync(0xffffffffu, (int)f, 1);
+    lx = __shfl_up_sync(0xffffffffu, acc, 1);
+    lxf = __shfl_up_sync(0xffffffffu, (int)f, 1);
     if (lane == 0) {
       lx = absent<T>();
       lxf = false;
@@ -611,10 +564,6 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
     if (lane == 31) sm.wt[w] = acc;
     if (SEG && lane == 31 && f) atomicOr(&sm.wtf, 1u << w);
     __syncthreads();
-
-    // ---- aggregate, publication, anchored look-back (warp 0); meanwhile
-    // warps 1..31 issue the copies of the next chunk into the free stage
-    if (w != 0 && next_from_stage) prefetch(cn, hb ^ 1, 32);
     if (w == 0) {
       T wa = sm.wt[lane];
       bool wf = SEG && ((sm.wtf >> lane) & 1u);
@@ -634,14 +583,117 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
         wx = absent<T>();
         wxf = false;
       }
-      sm.wx[lane] = wx;
+      sm.wx[set][lane] = wx;
       const unsigned int wxm = __ballot_sync(0xffffffffu, wxf);
       const T agg = __shfl_sync(0xffffffffu, wa, 31);
-      const bool aggf = __shfl_sync(0xffffffffu, (int)wf, 31);
       if (lane == 0) {
-        sm.wxf = wxm;
+        sm.wxf[set] = wxm;
+        sm.wtf = 0u;   // read above; reset for the next phase 1
         publish<T>(a.desc + c, agg);
       }
+    }
+  };
+
+  if (blockIdx.x == 0) {   // CTA 0 runs the anchor chain
+    if (w == 0) anchor_chain<T, SEG>(a);
+    return;
+  }
+  // worker CTA i takes chunks i-1, i-1+(G-1), ... (cooperative launch: all resident)
+  const long long stride = gridDim.x - 1;
+  long long c = blockIdx.x - 1;
+  if (c >= a.nchunks) return;
+
+  T x[E];
+  int hb = 0, set = 0;
+  T lx;
+  bool lxf;
+  if (tid == 0) sm.wtf = 0u;
+  // ---- prologue: chunk c into registers, its phase 1
+  if (can_prefetch(c)) {
+    prefetch(c, hb, 0);
+    cp_async_wait_all();
+    __syncthreads();
+    row_to_regs<T, E, REV>(stage + tid * ROW, x);
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const long long t = (long long)c * C + t0 + e;
+      x[e] = t < a.n ? a.x[gidx(c, t0 + e)] : absent<T>();
+    }
+    load_heads(c, hb);
+  }
+  __syncthreads();
+  {
+    T acc = x[0];
+    bool f = head_of(hb, t0);
+#pragma unroll
+    for (int e = 1; e < E; ++e) {
+      bool fr;
+      segop<T, SEG>(f, acc, head_of(hb, t0 + e), x[e], fr, acc);
+      f = fr;
+    }
+    finish_phase1(acc, f, set, c, lx, lxf);
+  }
+  long long cn = c + stride;
+  bool next_staged = cn < a.nchunks && can_prefetch(cn);
+  if (next_staged) prefetch(cn, hb ^ 1, 0);
+  long long pend_pos = -1, pend_chunk = 0;   // deferred first element of an exclusive chunk (thread 0)
+
+  while (true) {
+    const bool have_next = cn < a.nchunks;
+    T lxn = absent<T>();
+    bool lxfn = false;
+    // ---- phase 1 of the next chunk, straight from the stage (or global)
+    if (have_next) {
+      if (next_staged) {
+        cp_async_wait_all();
+      } else {
+        load_heads(cn, hb ^ 1);
+      }
+      __syncthreads();
+      T acc = absent<T>();
+      bool f = false;
+      if (next_staged) {
+        const T* row = stage + tid * ROW;
+#pragma unroll
+        for (int q = 0; q < E / PER16; ++q) {
+          const int qq = REV ? E / PER16 - 1 - q : q;
+          const float4 v4 = reinterpret_cast<const float4*>(row)[qq];
+          const T* pv = reinterpret_cast<const T*>(&v4);
+#pragma unroll
+          for (int k = 0; k < PER16; ++k) {
+            const int e = q * PER16 + k;
+            const T xe = REV ? pv[PER16 - 1 - k] : pv[k];
+            if (e == 0) {
+              acc = xe;
+              f = head_of(hb ^ 1, t0);
+            } else {
+              bool fr;
+              segop<T, SEG>(f, acc, head_of(hb ^ 1, t0 + e), xe, fr, acc);
+              f = fr;
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const long long t = (long long)cn * C + t0 + e;
+          const T xe = t < a.n ? a.x[gidx(cn, t0 + e)] : absent<T>();
+          if (e == 0) {
+            acc = xe;
+            f = head_of(hb ^ 1, t0);
+          } else {
+            bool fr;
+            segop<T, SEG>(f, acc, head_of(hb ^ 1, t0 + e), xe, fr, acc);
+            f = fr;
+          }
+        }
+      }
+      finish_phase1(acc, f, set ^ 1, cn, lxn, lxfn);
+    }
+
+    // ---- anchored look-back of the current chunk (warp 0)
+    if (w == 0) {
       const long long k = c / 32;
       const int j = (int)(c % 32);
       T v = absent<T>();
@@ -655,11 +707,11 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
         vf = SEG;
       }
 #pragma unroll
-      for (int s = 1; s < 32; s <<= 1) {
-        const T o = __shfl_xor_sync(0xffffffffu, v, s);
-        const bool of = __shfl_xor_sync(0xffffffffu, (int)vf, s);
+      for (int s2 = 1; s2 < 32; s2 <<= 1) {
+        const T o = __shfl_xor_sync(0xffffffffu, v, s2);
+        const bool of = __shfl_xor_sync(0xffffffffu, (int)vf, s2);
         bool fr;
-        if (lane & s)
+        if (lane & s2)
           segop<T, SEG>(vf, v, of, o, fr, v);
         else
           segop<T, SEG>(of, o, vf, v, fr, v);
@@ -669,19 +721,20 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
         sm.excl = v;
         sm.exclf = vf;
       }
-      (void)aggf;
     }
     __syncthreads();
 
-    // ---- phase 2: element values (inclusive), in place in x
+    // ---- phase 2 of the current chunk: element values, in place in x
+    const long long base = c * C;
+    const long long nvalid = min((long long)C, a.n - base);
     {
       bool f1, f2;
       T y;
-      segop<T, SEG>(SEG && sm.exclf, sm.excl, SEG && ((sm.wxf >> w) & 1u), sm.wx[w], f1, y);
+      segop<T, SEG>(SEG && sm.exclf, sm.excl, SEG && ((sm.wxf[set] >> w) & 1u), sm.wx[set][w], f1, y);
       segop<T, SEG>(f1, y, lxf, lx, f2, y);
 #pragma unroll
       for (int e = 0; e < E; ++e) {
-        y = (SEG && head(t0 + e)) ? x[e] : y + x[e];
+        y = (SEG && head_of(hb, t0 + e)) ? x[e] : y + x[e];
         x[e] = y;
       }
     }
@@ -695,27 +748,18 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
         if (e == want) tv = x[e];
       *a.total_out = tv;
     }
-
-    // ---- outputs
     const bool full = nvalid == C;
-    if (!EXCL) {
-      const long long g0 = REV ? a.n - base - t0 - E : base + t0;
-      if (full && (reinterpret_cast<uintptr_t>(a.y + g0) & 31) == 0) {
-        regs_to_global_256<T, E, REV>(a.y + g0, x);
-      } else {
-#pragma unroll
-        for (int e = 0; e < E; ++e)
-          if (t0 + e < nvalid) a.y[gidx(c, t0 + e)] = x[e];
-      }
-    } else {
+    if (EXCL) {
       // previous inclusive value for this lane's first element
       if (lane == 31) sm.last[w] = x[E - 1];
       T pl = __shfl_up_sync(0xffffffffu, x[E - 1], 1);
       __syncthreads();
       if (lane == 0) pl = (w > 0) ? sm.last[w - 1] : T(0.0);   // chunk start: written later
 #pragma unroll
-      for (int e = E - 1; e > 0; --e) x[e] = (SEG && head(t0 + e)) ? T(0.0) : x[e - 1];
-      x[0] = (SEG && head(t0)) ? T(0.0) : pl;
+      for (int e = E - 1; e > 0; --e) x[e] = (SEG && head_of(hb, t0 + e)) ? T(0.0) : x[e - 1];
+      x[0] = (SEG && head_of(hb, t0)) ? T(0.0) : pl;
+    }
+    {
       const long long g0 = REV ? a.n - base - t0 - E : base + t0;
       if (full && (reinterpret_cast<uintptr_t>(a.y + g0) & 31) == 0) {
         regs_to_global_256<T, E, REV>(a.y + g0, x);
@@ -724,28 +768,44 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
         for (int e = 0; e < E; ++e)
           if (t0 + e < nvalid) a.y[gidx(c, t0 + e)] = x[e];
       }
-      if (tid == 0) {
-        // the chunk's first element is the previous chunk's last inclusive
-        // value: resolve the one deferred from the chunk before this one,
-        // then defer this one (its predecessor may still be writing)
-        if (pend_pos >= 0) {
-          T v;
-          wait_value<T>(a.tails + (pend_chunk - 1), v, a.status, a.timeout_ns);
-          a.y[pend_pos] = v;
-        }
-        pend_pos = -1;
-        if (c > 0 && !(SEG && head(0))) {
-          pend_pos = gidx(c, 0);
-          pend_chunk = c;
-        }
+    }
+    if (EXCL && tid == 0) {
+      // the chunk's first element is the previous chunk's last inclusive
+      // value: resolve the one deferred from the chunk before this one, then
+      // defer this one (its predecessor may still be writing)
+      if (pend_pos >= 0) {
+        T v;
+        wait_value<T>(a.tails + (pend_chunk - 1), v, a.status, a.timeout_ns);
+        a.y[pend_pos] = v;
+      }
+      pend_pos = -1;
+      if (c > 0 && !(SEG && head_of(hb, 0))) {
+        pend_pos = gidx(c, 0);
+        pend_chunk = c;
       }
     }
 
-    if (cn >= a.nchunks) break;
+    if (!have_next) break;
+    __syncthreads();   // this chunk's shared data is no longer read
+    // ---- promote the next chunk to registers; prefetch the one after
+    if (next_staged) {
+      row_to_regs<T, E, REV>(stage + tid * ROW, x);
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const long long t = (long long)cn * C + t0 + e;
+        x[e] = t < a.n ? a.x[gidx(cn, t0 + e)] : absent<T>();
+      }
+    }
+    __syncthreads();   // stage free
     c = cn;
-    cur_from_stage = next_from_stage;
-    hb ^= next_from_stage ? 1 : 0;
-    __syncthreads();   // shared arrays of this chunk are no longer read
+    hb ^= 1;
+    set ^= 1;
+    lx = lxn;
+    lxf = lxfn;
+    cn = c + stride;
+    next_staged = cn < a.nchunks && can_prefetch(cn);
+    if (next_staged) prefetch(cn, hb ^ 1, 0);
   }
   if (EXCL && tid == 0 && pend_pos >= 0) {
     T v;
