@@ -32,6 +32,21 @@ template <typename T> __device__ __forceinline__ T absent() { return T(-0.0); }
 // ---------------------------------------------------------------------------
 // 256-bit loads (one 32-byte sector per lane).  The pointer must be 32-byte
 // aligned.  Read-only path; the data are not written by the same kernel.
+// Bulk prefetch of the byte range [p, p + bytes) into L2 by the copy engine
+// (cp.async.bulk.prefetch.L2), in 4 KB pieces spread over threads
+// [0, nthreads) of the caller's group.  Both ends are widened to 16-byte
+// boundaries; every widened block still holds a byte of the range, so it lies
+// in mapped memory.  A prefetch changes no data, only where it is cached.
+__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes, int me, int nthreads) {
+  if (bytes == 0) return;
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p) & ~(uintptr_t)15;
+  const uintptr_t hi = (reinterpret_cast<uintptr_t>(p) + bytes + 15) & ~(uintptr_t)15;
+  for (uintptr_t q = lo + (uintptr_t)me * 4096; q < hi; q += (uintptr_t)nthreads * 4096) {
+    const unsigned sz = (unsigned)((hi - q) < 4096 ? (hi - q) : 4096);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(q), "r"(sz) : "memory");
+  }
+}
+
 __device__ __forceinline__ void ld_nc_256(const float* p, float (&v)[8]) {
   asm volatile("ld.global.nc.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),

@@ -643,6 +643,48 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
     const bool have_next = cn < a.nchunks;
     T lxn = absent<T>();
     bool lxfn = false;
+    {
+      // the chunk after next is copied into the stage only at the end of this
+      // iteration; move it from HBM into L2 now (warp 1: warp 0 runs the look-back)
+      const long long cn2 = cn + stride;
+      if (cn2 < a.nchunks && w == 1) {
+        const long long lo = cn2 * C, hi = min(a.n, lo + C);
+        prefetch_l2(a.x + (REV ? a.n - hi : lo), (size_t)(hi - lo) * sizeof(T), lane, 32);
+        if (SEG) prefetch_l2(a.head_bits + lo / 32, (size_t)((hi - lo + 31) / 32) * 4, lane, 32);
+      }
+    }
+    // ---- anchored look-back of the current chunk (warp 0).  Its inputs were
+    // published during the previous iteration; it runs while the stage fills.
+    if (w == 0) {
+      const long long k = c / 32;
+      const int j = (int)(c % 32);
+      T v = absent<T>();
+      bool vf = false;
+      if (lane < j) {
+        const long long q = c - 1 - lane;
+        wait_value<T>(a.desc + q, v, a.status, a.timeout_ns);
+        vf = SEG && a.has_head[q];
+      } else if (lane == j && k > 0) {
+        wait_value<T>(a.anchors + (k - 1), v, a.status, a.timeout_ns);
+        vf = SEG;
+      }
+#pragma unroll
+      for (int s2 = 1; s2 < 32; s2 <<= 1) {
+        const T o = __shfl_xor_sync(0xffffffffu, v, s2);
+        const bool of = __shfl_xor_sync(0xffffffffu, (int)vf, s2);
+        bool fr;
+        if (lane & s2)
+          segop<T, SEG>(vf, v, of, o, fr, v);
+        else
+          segop<T, SEG>(of, o, vf, v, fr, v);
+        vf = fr;
+      }
+      if (lane == 0) {
+        sm.excl = v;
+        sm.exclf = vf;
+      }
+    }
+
     // ---- phase 1 of the next chunk, straight from the stage (or global)
     if (have_next) {
       if (next_staged) {
@@ -692,37 +734,7 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
       finish_phase1(acc, f, set ^ 1, cn, lxn, lxfn);
     }
 
-    // ---- anchored look-back of the current chunk (warp 0)
-    if (w == 0) {
-      const long long k = c / 32;
-      const int j = (int)(c % 32);
-      T v = absent<T>();
-      bool vf = false;
-      if (lane < j) {
-        const long long q = c - 1 - lane;
-        wait_value<T>(a.desc + q, v, a.status, a.timeout_ns);
-        vf = SEG && a.has_head[q];
-      } else if (lane == j && k > 0) {
-        wait_value<T>(a.anchors + (k - 1), v, a.status, a.timeout_ns);
-        vf = SEG;
-      }
-#pragma unroll
-      for (int s2 = 1; s2 < 32; s2 <<= 1) {
-        const T o = __shfl_xor_sync(0xffffffffu, v, s2);
-        const bool of = __shfl_xor_sync(0xffffffffu, (int)vf, s2);
-        bool fr;
-        if (lane & s2)
-          segop<T, SEG>(vf, v, of, o, fr, v);
-        else
-          segop<T, SEG>(of, o, vf, v, fr, v);
-        vf = fr;
-      }
-      if (lane == 0) {
-        sm.excl = v;
-        sm.exclf = vf;
-      }
-    }
-    __syncthreads();
+    __syncthreads();   // Excl(c) and the warp prefixes of c visible
 
     // ---- phase 2 of the current chunk: element values, in place in x
     const long long base = c * C;

@@ -244,6 +244,12 @@ __global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
   const long long tile_base = tile * K;
   if (tile_base >= N) return;
   const long long wbase = tile_base + (long long)warp * 32 * kIPT;
+  {
+    // the payloads are read after the ranking: start moving them into L2 now
+    const long long cnt = min(K, N - tile_base);
+    if (VB) prefetch_l2(reinterpret_cast<const unsigned char*>(a.vals_in) + tile_base * VB, (size_t)cnt * VB, tid, 32);
+    if (IDX && !FIRST) prefetch_l2(a.idx_in + tile_base, (size_t)cnt * 4, tid, 32);
+  }
 
   // digit starts (from the column totals) plus this tile's column prefixes
   digit_starts(a.totals, ndig, gbase, wsum);
@@ -450,6 +456,7 @@ __device__ T warp_pt_range(const T* __restrict__ p, long long len) {
   const int lane = threadIdx.x & 31;
   NodeCounter<T, 8> nc;
   const long long rounds = (len + 255) / 256;
+  if (rounds > 1) prefetch_l2(p, (size_t)len * sizeof(T), lane, 32);   // later rounds then come from L2
   for (long long r = 0; r < rounds; ++r) {
     T v[8];
     const long long b = r * 256 + lane * 8;
