@@ -54,6 +54,7 @@ __device__ __forceinline__ unsigned record_digit(const PassArgs& a, long long i,
   if (i >= N) return 0xffffffffu;
   const int32_t raw = LAST_USE ? __ldcs(a.keys_in + i) : __ldg(a.keys_in + i);
   if (FIRST) {
+    if (a.key_offset == 0) return (unsigned)raw < (unsigned long long)a.m ? ((unsigned)raw >> a.shift) & mask : 0xffffffffu;
     const long long k = (long long)raw + a.key_offset;
     return (k >= 0 && k < a.m) ? ((unsigned)k >> a.shift) & mask : 0xffffffffu;
   }
@@ -67,7 +68,7 @@ __device__ __forceinline__ unsigned record_digit(const PassArgs& a, long long i,
 // (records sharing lane 0's digit are added by one atomic, so a hot digit
 // does not serialise on one address).
 template <bool FIRST>
-__global__ void __launch_bounds__(256) sort_count_kernel(PassArgs a, long long K) {
+__global__ void __launch_bounds__(256, 8) sort_count_kernel(PassArgs a, long long K) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned int* cnt = reinterpret_cast<unsigned int*>(smem_raw);   // [ndig]
   const int tid = threadIdx.x, lane = tid & 31;
@@ -82,21 +83,22 @@ __global__ void __launch_bounds__(256) sort_count_kernel(PassArgs a, long long K
     unsigned d = 0xffffffffu;
     if (in) {
       if (FIRST) {
-        const long long kk = (long long)k + a.key_offset;
-        if (kk >= 0 && kk < a.m) d = ((unsigned)kk >> a.shift) & mask;
+        if (a.key_offset == 0) {
+          if ((unsigned)k < (unsigned long long)a.m) d = ((unsigned)k >> a.shift) & mask;
+        } else {
+          const long long kk = (long long)k + a.key_offset;
+          if (kk >= 0 && kk < a.m) d = ((unsigned)kk >> a.shift) & mask;
+        }
       } else {
         d = ((unsigned)k >> a.shift) & mask;
       }
     }
     const bool valid = d != 0xffffffffu;
     const unsigned d0 = __shfl_sync(0xffffffffu, d, 0);
-    const bool in0 = valid && d == d0;
-    const unsigned same0 = __ballot_sync(0xffffffffu, in0);
-    if (in0) {
-      if (lane == __ffs(same0) - 1) atomicAdd(&cnt[d], (unsigned)__popc(same0));
-    } else if (valid) {
-      atomicAdd(&cnt[d], 1u);
-    }
+    const unsigned same0 = __ballot_sync(0xffffffffu, valid && d == d0);
+    // lane 0 adds its whole digit group; the other lanes add themselves (if
+    // lane 0 is invalid, d0 matches no valid digit)
+    if (valid && (d != d0 || lane == 0)) atomicAdd(&cnt[d], d == d0 ? (unsigned)__popc(same0) : 1u);
   };
   if (t0 < t1) {
     const bool vec = (reinterpret_cast<uintptr_t>(a.keys_in + t0) & 15) == 0;
@@ -209,6 +211,16 @@ __device__ __forceinline__ void digit_starts(const unsigned int* totals, int ndi
   __syncthreads();
 }
 
+// 4- or 8-byte asynchronous copy global -> shared (both naturally aligned).
+template <int BYTES>
+__device__ __forceinline__ void cp_async_small(void* smem, const void* gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(sa), "l"(gmem), "n"(BYTES) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+}
+
 template <int VB> struct Payload;
 template <> struct Payload<0> { using U = unsigned int; };
 template <> struct Payload<4> { using U = unsigned int; };
@@ -226,7 +238,7 @@ __host__ __device__ inline size_t pass_front_bytes(int nwarps, int ndig, long lo
 }
 
 template <int VB, bool FIRST, bool IDX, bool KEYS_OUT, bool STAGE>
-__global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
+__global__ void __launch_bounds__(256, 3) sort_pass_kernel(PassArgs a) {
   using U = typename Payload<VB>::U;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
@@ -251,6 +263,12 @@ __global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
     if (IDX && !FIRST) prefetch_l2(a.idx_in + tile_base, (size_t)cnt * 4, tid, 32);
   }
 
+  // ---- this warp's digits: all loads in flight while the digit starts are
+  // formed; record order = (round, lane) = input order
+  unsigned packed[kIPT];
+#pragma unroll
+  for (int r = 0; r < kIPT; ++r) packed[r] = record_digit<FIRST, true>(a, wbase + (long long)r * 32 + lane, N, mask);
+
   // digit starts (from the column totals) plus this tile's column prefixes
   digit_starts(a.totals, ndig, gbase, wsum);
   for (int d = tid; d < ndig; d += blockDim.x) gbase[d] += a.counts[tile * ndig + d];
@@ -260,11 +278,7 @@ __global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
   }
   __syncwarp();
 
-  // ---- load this warp's digits (all loads in flight), then rank inside the
-  // warp; record order = (round, lane) = input order
-  unsigned packed[kIPT];
-#pragma unroll
-  for (int r = 0; r < kIPT; ++r) packed[r] = record_digit<FIRST, true>(a, wbase + (long long)r * 32 + lane, N, mask);
+  // ---- rank inside the warp
   // The lanes of a round that share a digit ("peers") are found without a
   // warp vote per digit bit: lanes with lane 0's digit by one ballot, the
   // others by OR-ing their lane bit into a per-warp mask word of their digit
@@ -388,30 +402,25 @@ __global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
   int32_t* __restrict__ iout = a.idx_out;
   const int32_t* __restrict__ kin = a.keys_in;
   int32_t* __restrict__ kout = a.keys_out;
-  constexpr int B = 4;
+  // payloads go from global memory (L2, prefetched above) straight to their
+  // sorted slot by asynchronous copies: no registers, one round trip
 #pragma unroll
-  for (int r0 = 0; r0 < kIPT; r0 += B) {
-    U vv[B];
-    int32_t ii[B], kk[B];
-#pragma unroll
-    for (int e = 0; e < B; ++e) {
-      const long long i = wbase + (long long)(r0 + e) * 32 + lane;
-      const bool ok = packed[r0 + e] != 0xffffffffu;
-      if (VB) vv[e] = ok ? __ldg(vin + i) : U(0);
-      if (IDX) ii[e] = ok ? (FIRST ? (int32_t)i : __ldg(iin + i)) : 0;
-      if (KEYS_OUT) kk[e] = ok ? (FIRST ? (int32_t)((long long)__ldg(kin + i) + a.key_offset) : __ldg(kin + i)) : 0;
+  for (int r = 0; r < kIPT; ++r) {
+    const unsigned pk = packed[r];
+    if (pk == 0xffffffffu) continue;
+    const long long i = wbase + (long long)r * 32 + lane;
+    const unsigned lp = pk & 0xffffu;
+    if (VB) cp_async_small<VB>(s_val + lp, vin + i);
+    if (IDX) {
+      if (FIRST)
+        s_idx[lp] = (int32_t)i;
+      else
+        cp_async_small<4>(s_idx + lp, iin + i);
     }
-#pragma unroll
-    for (int e = 0; e < B; ++e) {
-      const unsigned pk = packed[r0 + e];
-      if (pk == 0xffffffffu) continue;
-      const unsigned lp = pk & 0xffffu;
-      if (VB) s_val[lp] = vv[e];
-      if (IDX) s_idx[lp] = ii[e];
-      if (KEYS_OUT) s_key[lp] = kk[e];
-      s_dig[lp] = (unsigned short)(pk >> 16);
-    }
+    if (KEYS_OUT) cp_async_small<4>(s_key + lp, kin + i);   // raw key; the offset is added on the way out
+    s_dig[lp] = (unsigned short)(pk >> 16);
   }
+  cp_async_commit_wait_all();
   __syncthreads();
   for (long long i = tid; i < nvalid_tile; i += blockDim.x) {
     const unsigned d = s_dig[i];
@@ -422,7 +431,7 @@ __global__ void __launch_bounds__(1024) sort_pass_kernel(PassArgs a) {
     }
     if (VB) vout[pos] = s_val[i];
     if (IDX) iout[pos] = s_idx[i];
-    if (KEYS_OUT) kout[pos] = s_key[i];
+    if (KEYS_OUT) kout[pos] = FIRST ? (int32_t)((long long)s_key[i] + a.key_offset) : s_key[i];
   }
 }
 
@@ -506,22 +515,48 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
   for (long long k = lane; k < nblk; k += 32) blocks[base + k] = (b << 24) | k;
 }
 
+// One CTA of 256 threads per rank-aligned 2048-record block of a long bin.
+// All leaves are read in one coalesced round into shared memory; thread t
+// then takes leaves [8t, 8t+8) (a level-3 node), the warp's butterfly gives
+// the level-8 node and the tree over the 8 warps the level-11 node -- the
+// same node as any other aligned decomposition of the block.
 template <typename T>
 __global__ void __launch_bounds__(256)
 segtree_blocks_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg, const long long* __restrict__ blocks,
                       const unsigned int* __restrict__ nblocks, T* __restrict__ nodes,
                       const unsigned int* __restrict__ n_valid, long long max_blocks) {
-  const long long q = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+  static_assert(kSegBlock == 256 * 8, "one CTA of 256 threads x 8 leaves per block");
+  __shared__ __align__(16) T buf[kSegBlock];
+  __shared__ T wnode[8];
+  const long long q = blockIdx.x;
   if (q >= (long long)*nblocks || q >= max_blocks) return;
+  const int tid = threadIdx.x;
   const long long e = blocks[q];
   const long long b = e >> 24, k = e & ((1 << 24) - 1);
   const long long N = *n_valid;
   const long long hi = min((long long)seg[b + 1], N);
   const long long lo = max(0LL, min((long long)seg[b] + k * kSegBlock, hi));
   const long long len = min((long long)kSegBlock, hi - lo);
-  const T t = warp_pt_range(vals + lo, len);
-  if (lane == 0) nodes[q] = t;
+#pragma unroll
+  for (int i = 0; i < kSegBlock / 256; ++i) {
+    const int j = i * 256 + tid;
+    buf[j] = j < len ? __ldg(vals + lo + j) : absent<T>();
+  }
+  __syncthreads();
+  constexpr int NQ = 8 * (int)sizeof(T) / 16;
+  float4 q4[NQ];
+#pragma unroll
+  for (int i = 0; i < NQ; ++i) q4[i] = reinterpret_cast<const float4*>(buf + tid * 8)[i];
+  T v[8];
+  memcpy(v, q4, sizeof(v));
+  const T node = warp_pt(thread_pt(v));
+  if ((tid & 31) == 0) wnode[tid >> 5] = node;
+  __syncthreads();
+  if (tid == 0) {
+    const T a01 = wnode[0] + wnode[1], a23 = wnode[2] + wnode[3];
+    const T a45 = wnode[4] + wnode[5], a67 = wnode[6] + wnode[7];
+    nodes[q] = (a01 + a23) + (a45 + a67);
+  }
 }
 
 template <typename T>
@@ -550,7 +585,11 @@ SortPlan make_sort_plan(long long n, long long m, int value_bytes, bool need_idx
   while ((1LL << B) < m) ++B;
   p.passes = B <= 10 ? 1 : (B + 9) / 10;
   p.digit_bits = B == 0 ? 1 : (B + p.passes - 1) / p.passes;
-  p.threads = block_threads ? block_threads : 256;
+  // The sort's tile is threads x kIPT records.  block_threads = 128 gives
+  // 4,096-record tiles; every other choice the 8,192-record tiles of 256
+  // threads (the ranking's per-warp digit arrays make larger CTAs pointless).
+  // Tiling never changes the bits: the sort is stable.
+  p.threads = block_threads == 128 ? 128 : 256;
   p.ipt = kIPT;
   const long long K = (long long)p.threads * kIPT;
   p.tiles = (n + K - 1) / K;
@@ -699,7 +738,7 @@ int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T*
       p.max_lsegs, &h->status);
   launch_end(s);
   launch_begin("det_segtree_blocks", s);
-  segtree_blocks_kernel<T><<<(unsigned)((p.max_blocks * 32 + 255) / 256), 256, 0, s>>>(
+  segtree_blocks_kernel<T><<<(unsigned)p.max_blocks, 256, 0, s>>>(
       sorted_vals, seg, blocks, &h->long_blocks, nodes, &h->n_valid, p.max_blocks);
   launch_end(s);
   launch_begin("det_segtree_long", s);

@@ -26,6 +26,8 @@
  *   CUDA graph.
  * - `block_threads` selects the CUDA block size: 0 (the default) or one of
  *   128, 256, 512, 1024.  It changes the launch shape only, never the bits.
+ *   The sorts behind the scatter calls use 128-thread CTAs when asked for
+ *   128 and 256-thread CTAs otherwise.
  * - Return value: DET_OK, or an error code for a bad argument found on the
  *   host (nothing is enqueued then), or DET_ERR_CUDA if a launch failed.
  *   Errors detected on the device (a look-back wait that gave up) are written
