@@ -32,7 +32,11 @@ sys.path.insert(0, ROOT)
 from deterministic_floating_point_gb300 import workloads  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
+# GB300's FP64 rate: 1.25 TFLOP/s nominal, an FMA counted as two operations,
+# i.e. 0.625 T adds/s -- two FP64 lanes per SM per clock on 152 SMs at 2,070 MHz.
+FP64_ADDS_PER_S = 152 * 2 * 2.07e9
 BLOCK_THREADS = 0      # --block-threads: launch shape of the library calls (never changes the bits)
+N_OVERRIDE = 0         # --n: element count of the sum and scan workloads (smaller cases for profiler captures)
 
 
 def load_peaks():
@@ -99,7 +103,7 @@ def build_workload(name, torch, det, dev):
     npdt = _np_dt(dt)
 
     if name.startswith("sum"):
-        n = workloads.SUM_N if name.startswith("sum_small") else 1 << 28
+        n = N_OVERRIDE or (workloads.SUM_N if name.startswith("sum_small") else 1 << 28)
         x_np = workloads.sum_input(n=n, dtype=npdt)
         x = torch.from_numpy(x_np).to(dev)
         out = torch.empty(1, dtype=tdt[dt], device=dev)
@@ -123,6 +127,7 @@ def build_workload(name, torch, det, dev):
             return m * reps, secs, f"{reps} x det_sum of the first {m} elements, 1 thread"
 
         return dict(state={"x": x, "out": out}, step=step, elems=n, algo_bytes=n * s, step_bytes=n * s,
+                    adds=(n - 1) if dt == "f64" else None,
                     dominant="det_sum",
                     dtype=dt, e2e_step=e2e_step, h2d=n * s, d2h=s, oracle_sample=oracle_sample,
                     config={"workload": f"det_sum n={n} uniform[0,12) {dt} seed 0", "n": n,
@@ -130,7 +135,7 @@ def build_workload(name, torch, det, dev):
 
     if name.startswith("scan") or name.startswith("segscan"):
         seg = name.startswith("segscan")
-        n = workloads.SCAN_SMALL_N if "small" in name else workloads.SCAN_N
+        n = N_OVERRIDE or (workloads.SCAN_SMALL_N if "small" in name else workloads.SCAN_N)
         x_np = workloads.scan_input(n=n, dtype=npdt)
         x = torch.from_numpy(x_np).to(dev)
         y = torch.empty_like(x)
@@ -168,6 +173,7 @@ def build_workload(name, torch, det, dev):
         kern = "det_segmented_scan" if seg else "det_scan"
         extra = " segments geometric(mean 4096)" if seg else ""
         return dict(state={"x": x, "y": y}, step=step, elems=n, algo_bytes=2 * n * s, step_bytes=2 * n * s,
+                    adds=(2 * n) if dt == "f64" else None,
                     dominant=kern,
                     dtype=dt, e2e_step=e2e_step, h2d=n * s, d2h=n * s, oracle_sample=oracle_sample,
                     config={"workload": f"{kern} forward inclusive n={n} lognormal(0,1) {dt} seed 4{extra}",
@@ -451,6 +457,9 @@ def measure_op(name, torch, det, dev, flush, steps, runs, peak):
            "kernel_GB_s": (wl["algo_bytes"] / (dom_ms * 1e-3) / 1e9) if dom_ms else None,
            "kernel_frac_of_peak": (wl["algo_bytes"] / (dom_ms * 1e-3) / 1e9 / peak) if dom_ms else None,
            "kernel_share": {k: round(sum(v) / sum(times), 4) for k, v in per_kernel.items()}}
+    if wl.get("adds") and dom_ms:
+        res["kernel_Gadd_s"] = wl["adds"] / (dom_ms * 1e-3) / 1e9
+        res["kernel_frac_of_fp64_add_peak"] = wl["adds"] / (dom_ms * 1e-3) / FP64_ADDS_PER_S
     res["distinct_results_det"] = len({wl["det_once"]() for _ in range(runs)})
     if "base_once" in wl:
         for _ in range(2):
@@ -520,6 +529,14 @@ def run_det(args, torch, rank, world):
                 "kernel_ms": dom_ms, "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                 "algo_bytes_per_launch": wl["algo_bytes"],
                 "kernel_share": {k: round(sum(v) / total_ms, 4) for k, v in per_kernel.items()}}
+    adds = wl.get("adds")
+    if adds and dom_ms and adds / FP64_ADDS_PER_S > wl["algo_bytes"] / (peak * 1e9):
+        # the FP64 add rate, not HBM, bounds this kernel: report against it
+        hbm = {k: roofline[k] for k in ("achieved", "peak", "unit", "frac", "peak_kind")}
+        a = adds / (dom_ms * 1e-3) / 1e9
+        roofline.update({"bound": "alu", "achieved": a, "peak": FP64_ADDS_PER_S / 1e9, "unit": "Gadd/s",
+                         "frac": a * 1e9 / FP64_ADDS_PER_S, "peak_kind": "nominal FP64 add rate",
+                         "algo_adds_per_launch": adds, "hbm": hbm})
 
     # end to end through host buffers (pinned), same metric
     for _ in range(2):
@@ -645,12 +662,15 @@ def main():
     ap.add_argument("--workload", default="scatter")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--block-threads", type=int, default=0)
+    ap.add_argument("--n", type=int, default=0,
+                    help="element count of the sum and scan workloads (default: the configured size)")
     ap.add_argument("--no-ops", dest="ops", action="store_false",
                     help="skip the other workloads measured beside the headline one")
     ap.add_argument("--runs", type=int, default=10, help="repeated runs for the distinct-result counts")
     args = ap.parse_args()
-    global BLOCK_THREADS
+    global BLOCK_THREADS, N_OVERRIDE
     BLOCK_THREADS = args.block_threads
+    N_OVERRIDE = args.n
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -587,9 +587,11 @@ SortPlan make_sort_plan(long long n, long long m, int value_bytes, bool need_idx
   p.digit_bits = B == 0 ? 1 : (B + p.passes - 1) / p.passes;
   // The sort's tile is threads x kIPT records.  block_threads = 128 gives
   // 4,096-record tiles; every other choice the 8,192-record tiles of 256
-  // threads (the ranking's per-warp digit arrays make larger CTAs pointless).
-  // Tiling never changes the bits: the sort is stable.
-  p.threads = block_threads == 128 ? 128 : 256;
+  // threads (the ranking's per-warp digit arrays make larger CTAs pointless),
+  // except that by default sorts of at most 2^22 records take the smaller
+  // tiles, so that they still spread over every SM.  Tiling never changes
+  // the bits: the sort is stable.
+  p.threads = (block_threads == 128 || (block_threads == 0 && n <= (1LL << 22))) ? 128 : 256;
   p.ipt = kIPT;
   const long long K = (long long)p.threads * kIPT;
   p.tiles = (n + K - 1) / K;
