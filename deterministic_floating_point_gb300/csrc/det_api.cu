@@ -64,6 +64,7 @@ extern "C" const char* det_status_string(int status) {
     case DET_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
     case DET_ERR_LOOKBACK_TIMEOUT: return "device: a look-back wait gave up";
     case DET_ERR_CUDA: return "CUDA call or launch failed";
+    case DET_ERR_COPY_TIMEOUT: return "device: a bulk copy into shared memory did not complete in time";
     default: return "unknown status";
   }
 }

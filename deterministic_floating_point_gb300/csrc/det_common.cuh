@@ -188,6 +188,54 @@ __device__ __forceinline__ void set_status(unsigned int* status, unsigned int co
   atomicCAS(status, 0u, code);
 }
 
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded on-device waits give up after this long (nanoseconds).
+constexpr unsigned long long kWaitNs = 2000000000ull;
+
+// ---------------------------------------------------------------------------
+// Bulk copies global -> shared by the copy engine, completed on an mbarrier
+// (CTA scope; a launch without clusters is a cluster of one CTA).
+__device__ __forceinline__ unsigned smem_u32(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// Arrive on bar (count 1) and add `bytes` to the transfer it waits for.
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+// dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsigned bytes, unsigned long long* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, unsigned parity) {
+  unsigned done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Wait until phase `parity` of bar has completed, for at most timeout_ns;
+// false if the wait gave up.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity, unsigned long long timeout_ns) {
+  const unsigned long long t0 = globaltimer();
+  unsigned polls = 0;
+  while (!mbar_try_wait(bar, parity))
+    if ((++polls & 255u) == 0 && globaltimer() - t0 > timeout_ns) return false;
+  return true;
+}
+
 // Host-side helpers -----------------------------------------------------------
 inline bool valid_block_threads(int bt) {
   return bt == 0 || bt == 128 || bt == 256 || bt == 512 || bt == 1024;

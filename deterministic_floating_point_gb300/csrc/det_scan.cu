@@ -72,11 +72,6 @@ __device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long lon
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 
 // Publish a value word.  The all-ones pattern marks "not yet published"; the
 // only value with those bits is a NaN, which is published as the canonical

@@ -49,16 +49,19 @@ struct PassArgs {
 // (first pass) its destination is outside [0, m).
 // The count kernel reads the keys with a normal cached load so that the
 // pass kernel, which reads them last, mostly finds them in L2.
-template <bool FIRST, bool LAST_USE>
-__device__ __forceinline__ unsigned record_digit(const PassArgs& a, long long i, long long N, unsigned mask) {
-  if (i >= N) return 0xffffffffu;
-  const int32_t raw = LAST_USE ? __ldcs(a.keys_in + i) : __ldg(a.keys_in + i);
+template <bool FIRST>
+__device__ __forceinline__ unsigned digit_of(const PassArgs& a, int32_t raw, unsigned mask) {
   if (FIRST) {
     if (a.key_offset == 0) return (unsigned)raw < (unsigned long long)a.m ? ((unsigned)raw >> a.shift) & mask : 0xffffffffu;
     const long long k = (long long)raw + a.key_offset;
     return (k >= 0 && k < a.m) ? ((unsigned)k >> a.shift) & mask : 0xffffffffu;
   }
   return ((unsigned)raw >> a.shift) & mask;
+}
+template <bool FIRST, bool LAST_USE>
+__device__ __forceinline__ unsigned record_digit(const PassArgs& a, long long i, long long N, unsigned mask) {
+  if (i >= N) return 0xffffffffu;
+  return digit_of<FIRST>(a, LAST_USE ? __ldcs(a.keys_in + i) : __ldg(a.keys_in + i), mask);
 }
 
 // counts[tile][d] = records of the tile with digit d.  The tile is the
@@ -263,11 +266,40 @@ __global__ void __launch_bounds__(256, 3) sort_pass_kernel(PassArgs a) {
     if (IDX && !FIRST) prefetch_l2(a.idx_in + tile_base, (size_t)cnt * 4, tid, 32);
   }
 
-  // ---- this warp's digits: all loads in flight while the digit starts are
-  // formed; record order = (round, lane) = input order
+  // ---- this tile's digits; record order = (round, lane) = input order.
+  // A full, aligned tile comes in by one bulk copy into the front of shared
+  // memory (the ranking arrays, zeroed only after the digit-start scan's
+  // barriers): 4-byte loads from every thread cannot keep enough requests in
+  // flight.  Other tiles use plain loads.
   unsigned packed[kIPT];
+  __shared__ __align__(8) unsigned long long keys_bar;
+  const bool bulk = (N - tile_base) >= K &&
+                    (size_t)K * 4 <= pass_front_bytes(nwarps, ndig, a.K, VB, IDX, KEYS_OUT, STAGE) &&
+                    (reinterpret_cast<uintptr_t>(a.keys_in + tile_base) & 15) == 0;
+  if (bulk) {
+    if (tid == 0) {
+      mbar_init(&keys_bar, 1);
+      mbar_arrive_expect_tx(&keys_bar, (unsigned)(K * 4));
+      bulk_copy_g2s(smem_raw, a.keys_in + tile_base, (unsigned)(K * 4), &keys_bar);
+    }
+    __syncthreads();   // the barrier is initialised before anyone waits on it
+    const bool ok = mbar_wait(&keys_bar, 0, kWaitNs);
+    if (__syncthreads_or(!ok)) {
+      // the copy did not complete: record it, give it (bounded) time to land, leave
+      if (tid == 0) {
+        set_status(a.status, DET_ERR_COPY_TIMEOUT);
+        mbar_wait(&keys_bar, 0, kWaitNs);
+      }
+      __syncthreads();
+      return;
+    }
+    const int32_t* sk = reinterpret_cast<const int32_t*>(smem_raw) + warp * 32 * kIPT;
 #pragma unroll
-  for (int r = 0; r < kIPT; ++r) packed[r] = record_digit<FIRST, true>(a, wbase + (long long)r * 32 + lane, N, mask);
+    for (int r = 0; r < kIPT; ++r) packed[r] = digit_of<FIRST>(a, sk[r * 32 + lane], mask);
+  } else {
+#pragma unroll
+    for (int r = 0; r < kIPT; ++r) packed[r] = record_digit<FIRST, true>(a, wbase + (long long)r * 32 + lane, N, mask);
+  }
 
   // digit starts (from the column totals) plus this tile's column prefixes
   digit_starts(a.totals, ndig, gbase, wsum);

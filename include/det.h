@@ -54,6 +54,7 @@ extern "C" {
 #define DET_ERR_WORKSPACE 4        /* workspace too small, or misaligned */
 #define DET_ERR_LOOKBACK_TIMEOUT 5 /* device: a look-back wait gave up (status word only) */
 #define DET_ERR_CUDA 6             /* a CUDA call or launch failed */
+#define DET_ERR_COPY_TIMEOUT 7     /* device: a bulk copy into shared memory did not complete in time (status word only) */
 
 /* scan flags */
 #define DET_SCAN_INCLUSIVE 0
@@ -211,8 +212,12 @@ int det_segmented_scan(const void* x, void* y, int64_t n, const int64_t* seg_off
 
 /* ------------------------------------------------------------------------
  * Status.  det_read_status synchronizes `stream`, then copies the device
- * status word out of `workspace` into *device_status (DET_OK or
- * DET_ERR_LOOKBACK_TIMEOUT).  Returns DET_OK or DET_ERR_CUDA.
+ * status word out of `workspace` into *device_status: DET_OK,
+ * DET_ERR_LOOKBACK_TIMEOUT or DET_ERR_COPY_TIMEOUT (a bounded wait gave up),
+ * or DET_ERR_INVALID_ARG (segment offsets found invalid on the device, or a
+ * sort position out of range -- the latter cannot happen for a correct
+ * ranking and is checked so that no write can leave its buffer).
+ * Returns DET_OK or DET_ERR_CUDA.
  */
 int det_read_status(const void* workspace, void* stream, int* device_status);
 const char* det_status_string(int status);
