@@ -43,6 +43,7 @@ struct PassArgs {
   unsigned int* totals;        // [ndig] column totals
   unsigned int* status;
   unsigned int* n_valid;
+  int32_t* seg_out;            // one-pass sorts: segment starts (m + 1), written by CTA 0 of the pass
 };
 
 // Digit of record i of a pass, or 0xffffffff if it is past the end or
@@ -134,34 +135,49 @@ __global__ void __launch_bounds__(256, 8) sort_count_kernel(PassArgs a, long lon
 }
 
 // For each digit column: exclusive prefix over tiles (in place) and the
-// column total.  CTA of 1024 threads = 32 digit lanes x 32 tile groups.
+// column total.  CTA of 1024 threads = 8 digit lanes x 128 tile groups (a
+// warp reads 8 consecutive digits of 4 tiles: whole 32-byte sectors).
+constexpr int kColDigits = 8, kColGroups = 128;
 __global__ void __launch_bounds__(1024) sort_colscan_kernel(PassArgs a, int count_valid) {
-  __shared__ unsigned int part[32][33];
-  const int dl = threadIdx.x & 31, g = threadIdx.x >> 5;
+  __shared__ unsigned int part[kColGroups][kColDigits + 1];
+  const int dl = threadIdx.x % kColDigits, g = threadIdx.x / kColDigits;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ndig = 1 << a.D;
-  const int d = blockIdx.x * 32 + dl;
+  const int d = blockIdx.x * kColDigits + dl;
   const long long T = a.tiles;
-  const long long TG = (T + 31) / 32;
+  const long long TG = (T + kColGroups - 1) / kColGroups;
   const long long t0 = g * TG, t1 = min(T, t0 + TG);
   unsigned sum = 0;
   if (d < ndig)
     for (long long t = t0; t < t1; ++t) sum += a.counts[t * ndig + d];
   part[g][dl] = sum;
   __syncthreads();
-  if (g == 0) {
-    // exclusive scan over the 32 groups of column dl (serial: 32 adds)
-    unsigned run = 0;
-    for (int k = 0; k < 32; ++k) {
-      const unsigned v = part[k][dl];
-      part[k][dl] = run;
-      run += v;
-    }
-    if (d < ndig) a.totals[d] = run;
-    if (count_valid) {
-      unsigned tot = d < ndig ? run : 0u;
+  if (warp < kColDigits) {
+    // exclusive scan over the 128 groups of digit column `warp`: 4 groups per lane
+    const int c = warp;
+    unsigned v[kColGroups / 32], loc = 0;
 #pragma unroll
-      for (int s = 16; s > 0; s >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, s);
-      if (dl == 0 && tot) atomicAdd(a.n_valid, tot);
+    for (int k = 0; k < kColGroups / 32; ++k) {
+      v[k] = part[lane * (kColGroups / 32) + k][c];
+      loc += v[k];
+    }
+    unsigned x = loc;
+#pragma unroll
+    for (int s2 = 1; s2 < 32; s2 <<= 1) {
+      const unsigned o = __shfl_up_sync(0xffffffffu, x, s2);
+      if (lane >= s2) x += o;
+    }
+    unsigned run = x - loc;
+#pragma unroll
+    for (int k = 0; k < kColGroups / 32; ++k) {
+      part[lane * (kColGroups / 32) + k][c] = run;
+      run += v[k];
+    }
+    const unsigned total = __shfl_sync(0xffffffffu, x, 31);
+    const int dc = blockIdx.x * kColDigits + c;
+    if (lane == 0 && dc < ndig) {
+      a.totals[dc] = total;
+      if (count_valid && total) atomicAdd(a.n_valid, total);
     }
   }
   __syncthreads();
@@ -303,6 +319,8 @@ __global__ void __launch_bounds__(256, 3) sort_pass_kernel(PassArgs a) {
 
   // digit starts (from the column totals) plus this tile's column prefixes
   digit_starts(a.totals, ndig, gbase, wsum);
+  if (tile == 0 && a.seg_out)   // digit = destination: the digit starts are the segment starts
+    for (long long b = tid; b <= a.m; b += blockDim.x) a.seg_out[b] = (int32_t)gbase[b];
   for (int d = tid; d < ndig; d += blockDim.x) gbase[d] += a.counts[tile * ndig + d];
   for (int d = lane; d < ndig; d += 32) {
     wcnt[warp * ndig + d] = 0;
@@ -452,11 +470,14 @@ __global__ void __launch_bounds__(256, 3) sort_pass_kernel(PassArgs a) {
     if (KEYS_OUT) cp_async_small<4>(s_key + lp, kin + i);   // raw key; the offset is added on the way out
     s_dig[lp] = (unsigned short)(pk >> 16);
   }
+  // global position = local position + (global digit start - local digit start)
+  for (int d = tid; d < ndig; d += blockDim.x) gbase[d] -= lstart[d];
   cp_async_commit_wait_all();
   __syncthreads();
+#pragma unroll 4
   for (long long i = tid; i < nvalid_tile; i += blockDim.x) {
     const unsigned d = s_dig[i];
-    const long long pos = (long long)gbase[d] + (i - (long long)lstart[d]);
+    const long long pos = (long long)gbase[d] + i;
     if (pos < 0 || pos >= a.n) {   // cannot happen for a correct ranking; never write out of bounds
       set_status(a.status, DET_ERR_INVALID_ARG);
       continue;
@@ -465,15 +486,6 @@ __global__ void __launch_bounds__(256, 3) sort_pass_kernel(PassArgs a) {
     if (IDX) iout[pos] = s_idx[i];
     if (KEYS_OUT) kout[pos] = FIRST ? (int32_t)((long long)s_key[i] + a.key_offset) : s_key[i];
   }
-}
-
-// seg[0..m] = exclusive scan of the digit totals of a one-pass sort.
-__global__ void __launch_bounds__(1024) sort_seg_from_totals_kernel(const unsigned int* __restrict__ totals, int ndig,
-                                                                   long long m, int32_t* __restrict__ seg) {
-  __shared__ unsigned int base[1025];
-  __shared__ unsigned int wsum[32];
-  digit_starts(totals, ndig, base, wsum);
-  for (long long b = threadIdx.x; b <= m; b += blockDim.x) seg[b] = (int32_t)base[b];
 }
 
 // seg[b] = first sorted position with key >= b, for b = 0..m (keys sorted).
@@ -492,17 +504,18 @@ __global__ void sort_bounds_kernel(const int32_t* __restrict__ keys, const unsig
 // PT over p[0..len) by one warp: rounds of 256 (8 per lane, in-register tree,
 // then five shuffle levels) combined by a binary counter (rounds are aligned
 // 256-blocks, i.e. nodes of level 8), collapsed by a right fold at the end.
-template <typename T>
+// COHERENT: read through L2 only (values written by other CTAs of the same launch).
+template <typename T, bool COHERENT = false>
 __device__ T warp_pt_range(const T* __restrict__ p, long long len) {
   const int lane = threadIdx.x & 31;
   NodeCounter<T, 8> nc;
   const long long rounds = (len + 255) / 256;
-  if (rounds > 1) prefetch_l2(p, (size_t)len * sizeof(T), lane, 32);   // later rounds then come from L2
+  if (!COHERENT && rounds > 1) prefetch_l2(p, (size_t)len * sizeof(T), lane, 32);   // later rounds then come from L2
   for (long long r = 0; r < rounds; ++r) {
     T v[8];
     const long long b = r * 256 + lane * 8;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = (b + e < len) ? __ldg(p + b + e) : absent<T>();
+    for (int e = 0; e < 8; ++e) v[e] = (b + e < len) ? (COHERENT ? __ldcg(p + b + e) : __ldg(p + b + e)) : absent<T>();
     nc.push(warp_pt(thread_pt(v)));   // node of the aligned 256-block r (level 8)
   }
   return nc.result();
@@ -517,9 +530,10 @@ struct LongSeg {
 template <typename T>
 __global__ void __launch_bounds__(256)
 segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg, long long m, T* __restrict__ out,
-                    long long* __restrict__ blocks, LongSeg* __restrict__ lsegs, unsigned int* __restrict__ nblocks,
-                    unsigned int* __restrict__ nlsegs, const unsigned int* __restrict__ n_valid, long long max_blocks,
-                    long long max_lsegs, unsigned int* __restrict__ status) {
+                    long long* __restrict__ blocks, LongSeg* __restrict__ lsegs, unsigned int* __restrict__ ldone,
+                    unsigned int* __restrict__ nblocks, unsigned int* __restrict__ nlsegs,
+                    const unsigned int* __restrict__ n_valid, long long max_blocks, long long max_lsegs,
+                    unsigned int* __restrict__ status) {
   const long long b = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (b >= m) return;
@@ -533,41 +547,51 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
     return;
   }
   const long long nblk = (len + kSegBlock - 1) / kSegBlock;
-  long long base = 0;
+  long long base = 0, sidx = 0;
   if (lane == 0) {
     base = atomicAdd(nblocks, (unsigned)nblk);
-    const unsigned s = atomicAdd(nlsegs, 1u);
-    if (s < max_lsegs && base + nblk <= max_blocks)
-      lsegs[s] = LongSeg{b, base, nblk};
-    else
+    sidx = atomicAdd(nlsegs, 1u);
+    if (sidx < max_lsegs && base + nblk <= max_blocks) {
+      lsegs[sidx] = LongSeg{b, base, nblk};
+      ldone[sidx] = 0u;
+    } else {
       set_status(status, DET_ERR_INVALID_ARG);
+    }
   }
   base = __shfl_sync(0xffffffffu, base, 0);
-  if (base + nblk > max_blocks) return;
-  for (long long k = lane; k < nblk; k += 32) blocks[base + k] = (b << 24) | k;
+  sidx = __shfl_sync(0xffffffffu, sidx, 0);
+  if (sidx >= max_lsegs || base + nblk > max_blocks) return;
+  for (long long k = lane; k < nblk; k += 32) blocks[base + k] = (sidx << 24) | k;
 }
 
 // One CTA of 256 threads per rank-aligned 2048-record block of a long bin.
 // All leaves are read in one coalesced round into shared memory; thread t
 // then takes leaves [8t, 8t+8) (a level-3 node), the warp's butterfly gives
 // the level-8 node and the tree over the 8 warps the level-11 node -- the
-// same node as any other aligned decomposition of the block.
+// same node as any other aligned decomposition of the block.  The CTA that
+// completes a bin's last block (a per-bin counter) forms the PT over the
+// bin's block nodes and adds it to out[bin]: who does it varies, the tree
+// does not.
 template <typename T>
 __global__ void __launch_bounds__(256)
 segtree_blocks_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg, const long long* __restrict__ blocks,
-                      const unsigned int* __restrict__ nblocks, T* __restrict__ nodes,
-                      const unsigned int* __restrict__ n_valid, long long max_blocks) {
+                      const unsigned int* __restrict__ nblocks, const LongSeg* __restrict__ lsegs,
+                      unsigned int* __restrict__ ldone, T* nodes, T* __restrict__ out,
+                      const unsigned int* __restrict__ n_valid, long long max_blocks, long long max_lsegs) {
   static_assert(kSegBlock == 256 * 8, "one CTA of 256 threads x 8 leaves per block");
   __shared__ __align__(16) T buf[kSegBlock];
   __shared__ T wnode[8];
+  __shared__ int last;
   const long long q = blockIdx.x;
   if (q >= (long long)*nblocks || q >= max_blocks) return;
   const int tid = threadIdx.x;
   const long long e = blocks[q];
-  const long long b = e >> 24, k = e & ((1 << 24) - 1);
+  const long long sidx = e >> 24, k = e & ((1 << 24) - 1);
+  if (sidx >= max_lsegs) return;
+  const LongSeg L = lsegs[sidx];
   const long long N = *n_valid;
-  const long long hi = min((long long)seg[b + 1], N);
-  const long long lo = max(0LL, min((long long)seg[b] + k * kSegBlock, hi));
+  const long long hi = min((long long)seg[L.bin + 1], N);
+  const long long lo = max(0LL, min((long long)seg[L.bin] + k * kSegBlock, hi));
   const long long len = min((long long)kSegBlock, hi - lo);
 #pragma unroll
   for (int i = 0; i < kSegBlock / 256; ++i) {
@@ -588,19 +612,15 @@ segtree_blocks_kernel(const T* __restrict__ vals, const int32_t* __restrict__ se
     const T a01 = wnode[0] + wnode[1], a23 = wnode[2] + wnode[3];
     const T a45 = wnode[4] + wnode[5], a67 = wnode[6] + wnode[7];
     nodes[q] = (a01 + a23) + (a45 + a67);
+    __threadfence();
+    last = atomicAdd(&ldone[sidx], 1u) == (unsigned)(L.nblk - 1);
   }
-}
-
-template <typename T>
-__global__ void __launch_bounds__(256)
-segtree_long_kernel(const LongSeg* __restrict__ lsegs, const unsigned int* __restrict__ nlsegs,
-                    const T* __restrict__ nodes, T* __restrict__ out, long long max_lsegs) {
-  const long long s = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (s >= (long long)*nlsegs || s >= max_lsegs) return;
-  const LongSeg L = lsegs[s];
-  const T t = warp_pt_range(nodes + L.base, L.nblk);
-  if (lane == 0) out[L.bin] = out[L.bin] + t;
+  __syncthreads();
+  if (last && tid < 32) {
+    __threadfence();
+    const T t = warp_pt_range<T, true>(nodes + L.base, L.nblk);
+    if (tid == 0) out[L.bin] = out[L.bin] + t;
+  }
 }
 
 }  // namespace
@@ -656,6 +676,8 @@ SortPlan make_sort_plan(long long n, long long m, int value_bytes, bool need_idx
   off = align_up(off + (size_t)p.max_blocks * 8, 256);
   p.lsegs = off;
   off = align_up(off + (size_t)p.max_lsegs * sizeof(LongSeg), 256);
+  p.ldone = off;
+  off = align_up(off + (size_t)p.max_lsegs * 4, 256);
   p.nodes = off;
   off = align_up(off + (size_t)p.max_blocks * 8, 256);
   p.total = off;
@@ -722,6 +744,7 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
     a.totals = totals;
     a.status = &h->status;
     a.n_valid = &h->n_valid;
+    a.seg_out = p.passes == 1 ? seg : nullptr;
     const size_t csmem = (size_t)ndig * 4;
     const long long K = (long long)p.threads * kIPT;
     launch_begin("det_sort_count", s);
@@ -731,7 +754,7 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
       sort_count_kernel<false><<<(unsigned)p.tiles, 256, csmem, s>>>(a, K);
     launch_end(s);
     launch_begin("det_sort_colscan", s);
-    sort_colscan_kernel<<<(unsigned)((ndig + 31) / 32), 1024, 0, s>>>(a, first ? 1 : 0);
+    sort_colscan_kernel<<<(unsigned)((ndig + kColDigits - 1) / kColDigits), 1024, 0, s>>>(a, first ? 1 : 0);
     launch_end(s);
     if (cudaGetLastError() != cudaSuccess) return DET_ERR_CUDA;
     const bool keys_out = p.passes > 1;
@@ -744,11 +767,7 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
       e = launch_pass<0>(a, first, p.need_idx, keys_out, p.threads, p.tiles, s);
     if (e != cudaSuccess) return DET_ERR_CUDA;
   }
-  if (p.passes == 1) {
-    launch_begin("det_sort_seg", s);
-    sort_seg_from_totals_kernel<<<1, 1024, 0, s>>>(totals, ndig, p.m, seg);
-    launch_end(s);
-  } else {
+  if (p.passes > 1) {   // one-pass sorts got their segment starts from the pass
     launch_begin("det_sort_bounds", s);
     sort_bounds_kernel<<<(unsigned)((p.n + 1 + 255) / 256), 256, 0, s>>>(
         reinterpret_cast<const int32_t*>(w + p.keys[*final_buf]), &h->n_valid, p.m, seg, p.n);
@@ -766,18 +785,16 @@ int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T*
   long long* blocks = reinterpret_cast<long long*>(w + p.blocks);
   LongSeg* lsegs = reinterpret_cast<LongSeg*>(w + p.lsegs);
   T* nodes = reinterpret_cast<T*>(w + p.nodes);
+  unsigned int* ldone = reinterpret_cast<unsigned int*>(w + p.ldone);
   launch_begin("det_segtree_bins", s);
   segtree_bins_kernel<T><<<(unsigned)((p.m * 32 + 255) / 256), 256, 0, s>>>(
-      sorted_vals, seg, p.m, out, blocks, lsegs, &h->long_blocks, &h->long_segs, &h->n_valid, p.max_blocks,
+      sorted_vals, seg, p.m, out, blocks, lsegs, ldone, &h->long_blocks, &h->long_segs, &h->n_valid, p.max_blocks,
       p.max_lsegs, &h->status);
   launch_end(s);
   launch_begin("det_segtree_blocks", s);
-  segtree_blocks_kernel<T><<<(unsigned)p.max_blocks, 256, 0, s>>>(
-      sorted_vals, seg, blocks, &h->long_blocks, nodes, &h->n_valid, p.max_blocks);
-  launch_end(s);
-  launch_begin("det_segtree_long", s);
-  segtree_long_kernel<T><<<(unsigned)((p.max_lsegs * 32 + 255) / 256), 256, 0, s>>>(lsegs, &h->long_segs, nodes, out,
-                                                                                    p.max_lsegs);
+  segtree_blocks_kernel<T><<<(unsigned)p.max_blocks, 256, 0, s>>>(sorted_vals, seg, blocks, &h->long_blocks, lsegs,
+                                                                   ldone, nodes, out, &h->n_valid, p.max_blocks,
+                                                                   p.max_lsegs);
   launch_end(s);
   return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
 }
