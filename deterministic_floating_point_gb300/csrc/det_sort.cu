@@ -268,6 +268,7 @@ __global__ void __launch_bounds__(256, 3) sort_pass_kernel(PassArgs a) {
   unsigned int* gbase = reinterpret_cast<unsigned int*>(
       smem_raw + pass_front_bytes(nwarps, ndig, a.K, VB, IDX, KEYS_OUT, STAGE));   // [ndig + 1]
   __shared__ unsigned int wsum[32];
+  __shared__ unsigned int n_digits;   // distinct digits of the tile
 
   const long long tile = blockIdx.x;
   const long long N = FIRST ? a.n : (long long)*a.n_valid;
@@ -318,6 +319,7 @@ __global__ void __launch_bounds__(256, 3) sort_pass_kernel(PassArgs a) {
   }
 
   // digit starts (from the column totals) plus this tile's column prefixes
+  if (tid == 0) n_digits = 0u;
   digit_starts(a.totals, ndig, gbase, wsum);
   if (tile == 0 && a.seg_out)   // digit = destination: the digit starts are the segment starts
     for (long long b = tid; b <= a.m; b += blockDim.x) a.seg_out[b] = (int32_t)gbase[b];
@@ -409,14 +411,19 @@ __global__ void __launch_bounds__(256, 3) sort_pass_kernel(PassArgs a) {
   // ---- per digit: exclusive prefix over the warps of this tile, and the
   // tile's digit counts
   unsigned int* lstart = gbase + (ndig + 1);   // [ndig + 1] tile-local digit starts
-  for (int d = tid; d < ndig; d += blockDim.x) {
-    unsigned run = 0;
-    for (int w = 0; w < nwarps; ++w) {
-      const unsigned c = wcnt[w * ndig + d];
-      wcnt[w * ndig + d] = (unsigned short)run;
-      run += c;
+  {
+    unsigned nz = 0;
+    for (int d = tid; d < ndig; d += blockDim.x) {
+      unsigned run = 0;
+      for (int w = 0; w < nwarps; ++w) {
+        const unsigned c = wcnt[w * ndig + d];
+        wcnt[w * ndig + d] = (unsigned short)run;
+        run += c;
+      }
+      lstart[d] = run;   // count for now; turned into starts below
+      nz += run != 0;
     }
-    lstart[d] = run;   // count for now; turned into starts below
+    if (nz) atomicAdd(&n_digits, nz);
   }
   __syncthreads();
   {
@@ -435,6 +442,58 @@ __global__ void __launch_bounds__(256, 3) sort_pass_kernel(PassArgs a) {
     packed[r] = (d << 16) | (lstart[d] + wcnt[warp * ndig + d] + (pk & 0xffffu));
   }
   __syncthreads();   // the peer-mask and counter words are free from here on
+
+  // ---- one-pass sorts of full, aligned tiles whose digit runs are long (16
+  // records or more on average, so that a warp's stores mostly fall in one
+  // run): the tile's values come in by one bulk copy (input order) into the
+  // freed front of shared memory, and each thread stores its records' values
+  // straight to their global places.  Short runs go through the staging below.
+  const size_t front_bytes = pass_front_bytes(nwarps, ndig, a.K, VB, IDX, KEYS_OUT, STAGE);
+  if (VB > 0 && !KEYS_OUT && (!IDX || FIRST) && (N - tile_base) >= K && (size_t)K * VB <= front_bytes &&
+      lstart[ndig] >= 16u * n_digits &&
+      (reinterpret_cast<uintptr_t>(reinterpret_cast<const unsigned char*>(a.vals_in) + tile_base * VB) & 15) == 0) {
+    __shared__ __align__(8) unsigned long long vals_bar;
+    if (tid == 0) {
+      // the front was last written by ordinary stores: order them before the copy engine's writes
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_init(&vals_bar, 1);
+      mbar_arrive_expect_tx(&vals_bar, (unsigned)(K * VB));
+      bulk_copy_g2s(smem_raw, reinterpret_cast<const unsigned char*>(a.vals_in) + tile_base * VB, (unsigned)(K * VB),
+                    &vals_bar);
+    }
+    // global position of each record: local position + (global - local digit start)
+#pragma unroll
+    for (int r = 0; r < kIPT; ++r) {
+      const unsigned pk = packed[r];
+      if (pk == 0xffffffffu) continue;
+      const unsigned d = pk >> 16;
+      packed[r] = gbase[d] - lstart[d] + (pk & 0xffffu);
+    }
+    __syncthreads();   // the barrier is initialised before anyone waits on it
+    const bool ok = mbar_wait(&vals_bar, 0, kWaitNs);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        set_status(a.status, DET_ERR_COPY_TIMEOUT);
+        mbar_wait(&vals_bar, 0, kWaitNs);
+      }
+      __syncthreads();
+      return;
+    }
+    const U* sv = reinterpret_cast<const U*>(smem_raw) + warp * 32 * kIPT;
+    U* __restrict__ vout = reinterpret_cast<U*>(a.vals_out);
+#pragma unroll
+    for (int r = 0; r < kIPT; ++r) {
+      const unsigned pos = packed[r];
+      if (pos == 0xffffffffu) continue;
+      if ((long long)pos >= a.n) {   // cannot happen for a correct ranking; never write out of bounds
+        set_status(a.status, DET_ERR_INVALID_ARG);
+        continue;
+      }
+      vout[pos] = sv[r * 32 + lane];
+      if (IDX) a.idx_out[pos] = (int32_t)(wbase + (long long)r * 32 + lane);
+    }
+    return;
+  }
 
   // ---- stage the records in shared memory in tile-sorted order, then write
   // each digit's run to its global place with consecutive threads on
