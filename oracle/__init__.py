@@ -57,6 +57,10 @@ def _load():
                 getattr(lib, f"oracle_scatter_add_rows_{sfx}").argtypes = [vp, i64, i64, vp, i64, vp, i64, vp]
                 getattr(lib, f"oracle_scan_{sfx}").argtypes = [vp, vp, i64, ctypes.c_int, vp]
                 getattr(lib, f"oracle_segmented_scan_{sfx}").argtypes = [vp, vp, i64, vp, i64, ctypes.c_int]
+                getattr(lib, f"oracle_scatter_sub_{sfx}").argtypes = [vp, i64, vp, vp, i64]
+                getattr(lib, f"oracle_scatter_minmax_{sfx}").argtypes = [vp, i64, vp, vp, i64, ctypes.c_int]
+            lib.oracle_scan_i32.argtypes = [vp, vp, i64, ctypes.c_int, vp]
+            lib.oracle_slot_alloc.argtypes = [vp, i64, vp, i64, vp, i64, vp]
             lib.oracle_scan_chunk_elems.restype = i64
             lib.oracle_scan_chunk_elems.argtypes = [ctypes.c_int]
             lib.oracle_scan_lane_elems.restype = i64
@@ -155,3 +159,60 @@ def det_segmented_scan(x: np.ndarray, offsets: np.ndarray, flags: int = SCAN_INC
                                                             offsets.size - 1, int(flags))
     _check(rc, "segmented_scan")
     return y
+
+
+def det_scatter_sub(out: np.ndarray, bins: np.ndarray, values: np.ndarray):
+    """out[b] + PT(-values of group b); returns the new out (``out`` unmodified)."""
+    values = np.ascontiguousarray(values)
+    sfx = _sfx(values.dtype)
+    res = np.array(out, dtype=values.dtype, copy=True)
+    bins = np.ascontiguousarray(bins, dtype=np.int32)
+    if bins.size != values.size:
+        raise ValueError("bins and values differ in length")
+    _check(getattr(_load(), f"oracle_scatter_sub_{sfx}")(_ptr(res), res.size, _ptr(bins), _ptr(values), values.size),
+           "scatter_sub")
+    return res
+
+
+def _scatter_minmax(out, bins, values, is_max):
+    values = np.ascontiguousarray(values)
+    sfx = _sfx(values.dtype)
+    res = np.array(out, dtype=values.dtype, copy=True)
+    bins = np.ascontiguousarray(bins, dtype=np.int32)
+    if bins.size != values.size:
+        raise ValueError("bins and values differ in length")
+    _check(getattr(_load(), f"oracle_scatter_minmax_{sfx}")(_ptr(res), res.size, _ptr(bins), _ptr(values),
+                                                            values.size, int(is_max)), "scatter_minmax")
+    return res
+
+
+def det_scatter_min(out: np.ndarray, bins: np.ndarray, values: np.ndarray):
+    """IEEE 754-2019 minimum of the old value and each group; returns the new out."""
+    return _scatter_minmax(out, bins, values, False)
+
+
+def det_scatter_max(out: np.ndarray, bins: np.ndarray, values: np.ndarray):
+    """IEEE 754-2019 maximum of the old value and each group; returns the new out."""
+    return _scatter_minmax(out, bins, values, True)
+
+
+def det_scan_i32(x: np.ndarray, exclusive: bool = False):
+    """int32 prefix sum (wrapping modulo 2^32); returns (y, total)."""
+    x = np.ascontiguousarray(x, dtype=np.int32)
+    y = np.empty_like(x)
+    total = np.zeros(1, dtype=np.int32)
+    _check(_load().oracle_scan_i32(_ptr(x), _ptr(y), x.size, 1 if exclusive else 0, _ptr(total)), "scan_i32")
+    return y, int(total[0])
+
+
+def det_slot_alloc(counter: np.ndarray, index: np.ndarray, count: np.ndarray | None = None, index_offset: int = 0):
+    """Thread-order slot allocation; returns (slots, new_counter) (``counter`` unmodified)."""
+    ctr = np.array(counter, dtype=np.int32, copy=True)
+    index = np.ascontiguousarray(index, dtype=np.int32)
+    cnt = None if count is None else np.ascontiguousarray(count, dtype=np.int32)
+    if cnt is not None and cnt.size != index.size:
+        raise ValueError("count must have one entry per record")
+    slots = np.empty(index.size, dtype=np.int32)
+    _check(_load().oracle_slot_alloc(_ptr(ctr), ctr.size, _ptr(index), int(index_offset), _ptr(cnt), index.size,
+                                     _ptr(slots)), "slot_alloc")
+    return slots, ctr

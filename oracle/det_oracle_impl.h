@@ -101,6 +101,66 @@ int FN(oracle_scatter_add)(T* out, int64_t m, const int32_t* bins, const T* valu
 }
 
 /* ---------------------------------------------------------------------- */
+/* det_scatter_sub: the deterministic form of wp.atomic_sub(out, bins[i],
+ * values[i]).  The values are negated and then added in det_scatter_add's
+ * fixed order: out[b] = out[b] + PT(-values of group b), groups as above
+ * (Warp "Deterministic Execution", "Pattern 1: Accumulation", table row
+ * atomic_sub: values are negated and added in a fixed order). */
+int FN(oracle_scatter_sub)(T* out, int64_t m, const int32_t* bins, const T* values, int64_t n)
+{
+    if (n < 0 || (n > 0 && !values)) return 1;
+    T* neg = (T*)malloc(((size_t)n + 1) * sizeof(T));
+    if (!neg) return 3;
+    for (int64_t i = 0; i < n; ++i) neg[i] = -values[i];
+    int rc = FN(oracle_scatter_add)(out, m, bins, neg, n, NULL, NULL);
+    free(neg);
+    return rc;
+}
+
+/* IEEE 754-2019 minimum / maximum: a NaN operand gives NaN (returned as the
+ * canonical quiet NaN: payloads are not promised), -0 orders below +0, else
+ * the smaller / larger operand.  Both are associative and commutative, so a
+ * group's result does not depend on the order it is combined in. */
+static T FN(ieee_minimum)(T a, T b)
+{
+    if (a != a || b != b) return (T)NAN;
+    if (a == b) return signbit(a) ? a : b;
+    return a < b ? a : b;
+}
+static T FN(ieee_maximum)(T a, T b)
+{
+    if (a != a || b != b) return (T)NAN;
+    if (a == b) return signbit(a) ? b : a;
+    return a > b ? a : b;
+}
+
+/* det_scatter_min / det_scatter_max: the deterministic form of
+ * wp.atomic_min / wp.atomic_max(out, bins[i], values[i]): values are grouped
+ * by destination and minimized (maximized), and the old value takes part:
+ * out[b] = op(out[b], op over group b) for non-empty groups; other entries
+ * are untouched (Warp "Deterministic Execution", "Pattern 1: Accumulation",
+ * table rows atomic_min and atomic_max).  Invalid bins are skipped as in
+ * det_scatter_add.  is_max selects the maximum. */
+int FN(oracle_scatter_minmax)(T* out, int64_t m, const int32_t* bins, const T* values, int64_t n, int is_max)
+{
+    if (m < 0 || n < 0 || (m > 0 && !out) || (n > 0 && (!bins || !values))) return 1;
+    if (n > 2147483647LL || m > 2147483647LL) return 2;
+    T* acc = (T*)malloc(((size_t)m + 1) * sizeof(T));
+    unsigned char* seen = (unsigned char*)calloc((size_t)m + 1, 1);
+    if (!acc || !seen) { free(acc); free(seen); return 3; }
+    for (int64_t i = 0; i < n; ++i) {   /* index order; any order gives the same result */
+        int64_t b = bins[i];
+        if (b < 0 || b >= m) continue;
+        if (!seen[b]) { acc[b] = values[i]; seen[b] = 1; continue; }
+        acc[b] = is_max ? FN(ieee_maximum)(acc[b], values[i]) : FN(ieee_minimum)(acc[b], values[i]);
+    }
+    for (int64_t b = 0; b < m; ++b)
+        if (seen[b]) out[b] = is_max ? FN(ieee_maximum)(out[b], acc[b]) : FN(ieee_minimum)(out[b], acc[b]);
+    free(acc); free(seen);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
 /* det_scatter_add_rows: the tile row scatter of warp.tile_atomic_add_indexed
  * (axis 0): source row s is added to destination row idx[s] + row_offset;
  * destinations outside [0, dst_rows) are skipped; repeated rows accumulate.
