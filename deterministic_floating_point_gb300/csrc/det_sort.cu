@@ -564,7 +564,8 @@ __global__ void sort_bounds_kernel(const int32_t* __restrict__ keys, const unsig
 // then five shuffle levels) combined by a binary counter (rounds are aligned
 // 256-blocks, i.e. nodes of level 8), collapsed by a right fold at the end.
 // COHERENT: read through L2 only (values written by other CTAs of the same launch).
-template <typename T, bool COHERENT = false>
+// NEG: the leaves are the negated values (absent padding stays -0.0).
+template <typename T, bool COHERENT = false, bool NEG = false>
 __device__ T warp_pt_range(const T* __restrict__ p, long long len) {
   const int lane = threadIdx.x & 31;
   NodeCounter<T, 8> nc;
@@ -574,7 +575,14 @@ __device__ T warp_pt_range(const T* __restrict__ p, long long len) {
     T v[8];
     const long long b = r * 256 + lane * 8;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = (b + e < len) ? (COHERENT ? __ldcg(p + b + e) : __ldg(p + b + e)) : absent<T>();
+    for (int e = 0; e < 8; ++e) {
+      if (b + e < len) {
+        const T x = COHERENT ? __ldcg(p + b + e) : __ldg(p + b + e);
+        v[e] = NEG ? -x : x;
+      } else {
+        v[e] = absent<T>();
+      }
+    }
     nc.push(warp_pt(thread_pt(v)));   // node of the aligned 256-block r (level 8)
   }
   return nc.result();
@@ -586,7 +594,10 @@ struct LongSeg {
   long long nblk;
 };
 
-template <typename T>
+// NEG: the tree is over the negated values (scatter-sub).  The leaves are
+// negated, not the result: an exact zero from cancellation is +0.0 either
+// way, so -PT(v) and PT(-v) can differ in the sign of a zero.
+template <typename T, bool NEG>
 __global__ void __launch_bounds__(256)
 segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg, long long m, T* __restrict__ out,
                     long long* __restrict__ blocks, LongSeg* __restrict__ lsegs, unsigned int* __restrict__ ldone,
@@ -601,7 +612,7 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
   const long long len = hi - lo;
   if (len <= 0) return;
   if (len <= kSegBlock) {
-    const T t = warp_pt_range(vals + lo, len);
+    const T t = warp_pt_range<T, false, NEG>(vals + lo, len);
     if (lane == 0) out[b] = out[b] + t;
     return;
   }
@@ -631,7 +642,7 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
 // completes a bin's last block (a per-bin counter) forms the PT over the
 // bin's block nodes and adds it to out[bin]: who does it varies, the tree
 // does not.
-template <typename T>
+template <typename T, bool NEG>
 __global__ void __launch_bounds__(256)
 segtree_blocks_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg, const long long* __restrict__ blocks,
                       const unsigned int* __restrict__ nblocks, const LongSeg* __restrict__ lsegs,
@@ -655,7 +666,7 @@ segtree_blocks_kernel(const T* __restrict__ vals, const int32_t* __restrict__ se
 #pragma unroll
   for (int i = 0; i < kSegBlock / 256; ++i) {
     const int j = i * 256 + tid;
-    buf[j] = j < len ? __ldg(vals + lo + j) : absent<T>();
+    buf[j] = j < len ? (NEG ? -__ldg(vals + lo + j) : __ldg(vals + lo + j)) : absent<T>();
   }
   __syncthreads();
   constexpr int NQ = 8 * (int)sizeof(T) / 16;
@@ -677,7 +688,7 @@ segtree_blocks_kernel(const T* __restrict__ vals, const int32_t* __restrict__ se
   __syncthreads();
   if (last && tid < 32) {
     __threadfence();
-    const T t = warp_pt_range<T, true>(nodes + L.base, L.nblk);
+    const T t = warp_pt_range<T, true>(nodes + L.base, L.nblk);   // nodes already hold the negated leaves
     if (tid == 0) out[L.bin] = out[L.bin] + t;
   }
 }
@@ -836,7 +847,7 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
 }
 
 template <typename T>
-int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T* out, cudaStream_t s) {
+int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T* out, cudaStream_t s, bool negate) {
   if (p.n == 0 || p.m == 0) return DET_OK;
   char* w = reinterpret_cast<char*>(ws);
   SortHdr* h = reinterpret_cast<SortHdr*>(ws);
@@ -846,19 +857,20 @@ int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T*
   T* nodes = reinterpret_cast<T*>(w + p.nodes);
   unsigned int* ldone = reinterpret_cast<unsigned int*>(w + p.ldone);
   launch_begin("det_segtree_bins", s);
-  segtree_bins_kernel<T><<<(unsigned)((p.m * 32 + 255) / 256), 256, 0, s>>>(
-      sorted_vals, seg, p.m, out, blocks, lsegs, ldone, &h->long_blocks, &h->long_segs, &h->n_valid, p.max_blocks,
-      p.max_lsegs, &h->status);
+  auto* kb = negate ? segtree_bins_kernel<T, true> : segtree_bins_kernel<T, false>;
+  kb<<<(unsigned)((p.m * 32 + 255) / 256), 256, 0, s>>>(sorted_vals, seg, p.m, out, blocks, lsegs, ldone,
+                                                         &h->long_blocks, &h->long_segs, &h->n_valid, p.max_blocks,
+                                                         p.max_lsegs, &h->status);
   launch_end(s);
   launch_begin("det_segtree_blocks", s);
-  segtree_blocks_kernel<T><<<(unsigned)p.max_blocks, 256, 0, s>>>(sorted_vals, seg, blocks, &h->long_blocks, lsegs,
-                                                                   ldone, nodes, out, &h->n_valid, p.max_blocks,
-                                                                   p.max_lsegs);
+  auto* kk = negate ? segtree_blocks_kernel<T, true> : segtree_blocks_kernel<T, false>;
+  kk<<<(unsigned)p.max_blocks, 256, 0, s>>>(sorted_vals, seg, blocks, &h->long_blocks, lsegs, ldone, nodes, out,
+                                            &h->n_valid, p.max_blocks, p.max_lsegs);
   launch_end(s);
   return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
 }
 
-template int enqueue_segmented_tree<float>(const SortPlan&, void*, const float*, float*, cudaStream_t);
-template int enqueue_segmented_tree<double>(const SortPlan&, void*, const double*, double*, cudaStream_t);
+template int enqueue_segmented_tree<float>(const SortPlan&, void*, const float*, float*, cudaStream_t, bool);
+template int enqueue_segmented_tree<double>(const SortPlan&, void*, const double*, double*, cudaStream_t, bool);
 
 }  // namespace det

@@ -54,6 +54,7 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
 // Segmented pairwise tree: out[b] = out[b] + PT(vals[seg[b] .. seg[b+1]))
 // for every non-empty b.  T is float or double.
 template <typename T>
-int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T* out, cudaStream_t s);
+int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T* out, cudaStream_t s,
+                           bool negate = false);
 
 }  // namespace det

@@ -40,6 +40,14 @@ _SIGNATURES = {
     "det_scan": (_int, [_vp, _vp, _i64, _int, _int, _vp, _vp, _sz, _int, _vp]),
     "det_segmented_scan_workspace_bytes": (_sz, [_i64, _i64, _int]),
     "det_segmented_scan": (_int, [_vp, _vp, _i64, _vp, _i64, _int, _int, _vp, _sz, _int, _vp]),
+    "det_scatter_sub": (_int, [_vp, _i64, _vp, _vp, _i64, _int, _vp, _vp, _vp, _sz, _int, _vp]),
+    "det_scatter_minmax_workspace_bytes": (_sz, [_i64, _int]),
+    "det_scatter_min": (_int, [_vp, _i64, _vp, _vp, _i64, _int, _vp, _sz, _int, _vp]),
+    "det_scatter_max": (_int, [_vp, _i64, _vp, _vp, _i64, _int, _vp, _sz, _int, _vp]),
+    "det_scan_i32_workspace_bytes": (_sz, [_i64]),
+    "det_scan_i32": (_int, [_vp, _vp, _i64, _int, _vp, _vp, _sz, _int, _vp]),
+    "det_slot_alloc_workspace_bytes": (_sz, [_i64, _i64]),
+    "det_slot_alloc": (_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _sz, _int, _vp]),
     "det_read_status": (_int, [_vp, _vp, ctypes.POINTER(_int)]),
     "det_status_string": (ctypes.c_char_p, [_int]),
     "det_profile_set_events": (_int, [_vp, _int]),
@@ -179,6 +187,89 @@ def det_scatter_add(out: torch.Tensor, bins: torch.Tensor, values: torch.Tensor,
                                  _ptr(seg_offsets_out), _ptr(ws), ws.numel(), block_threads,
                                  _stream(stream)), "det_scatter_add")
     return out
+
+
+def det_scatter_sub(out: torch.Tensor, bins: torch.Tensor, values: torch.Tensor, *,
+                    perm_out: torch.Tensor | None = None, seg_offsets_out: torch.Tensor | None = None,
+                    block_threads: int = 0, workspace: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """out[bins[i]] -= values[i]: the values negated and added in det_scatter_add's order; returns out."""
+    _dev(out, "out"), _dev(bins, "bins"), _dev(values, "values")
+    code = _code(values)
+    if out.dtype != values.dtype or bins.dtype != torch.int32:
+        raise TypeError("out must match values' dtype and bins must be int32")
+    n, m = values.numel(), out.numel()
+    if bins.numel() != n:
+        raise ValueError("bins and values differ in length")
+    nbytes = lib().det_scatter_add_workspace_bytes(n, m, code)
+    ws = _ws(workspace, nbytes, values.device)
+    _check(lib().det_scatter_sub(_ptr(out), m, _ptr(bins), _ptr(values), n, code, _ptr(perm_out),
+                                 _ptr(seg_offsets_out), _ptr(ws), ws.numel(), block_threads,
+                                 _stream(stream)), "det_scatter_sub")
+    return out
+
+
+def _scatter_minmax(fn, out, bins, values, block_threads, workspace, stream):
+    _dev(out, "out"), _dev(bins, "bins"), _dev(values, "values")
+    code = _code(values)
+    if out.dtype != values.dtype or bins.dtype != torch.int32:
+        raise TypeError("out must match values' dtype and bins must be int32")
+    n, m = values.numel(), out.numel()
+    if bins.numel() != n:
+        raise ValueError("bins and values differ in length")
+    ws = _ws(workspace, lib().det_scatter_minmax_workspace_bytes(m, code), values.device)
+    _check(getattr(lib(), fn)(_ptr(out), m, _ptr(bins), _ptr(values), n, code, _ptr(ws), ws.numel(),
+                              block_threads, _stream(stream)), fn)
+    return out
+
+
+def det_scatter_min(out: torch.Tensor, bins: torch.Tensor, values: torch.Tensor, *, block_threads: int = 0,
+                    workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[b] = IEEE minimum of out[b] and the values aimed at b (see det.h); returns out."""
+    return _scatter_minmax("det_scatter_min", out, bins, values, block_threads, workspace, stream)
+
+
+def det_scatter_max(out: torch.Tensor, bins: torch.Tensor, values: torch.Tensor, *, block_threads: int = 0,
+                    workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[b] = IEEE maximum of out[b] and the values aimed at b (see det.h); returns out."""
+    return _scatter_minmax("det_scatter_max", out, bins, values, block_threads, workspace, stream)
+
+
+def det_scan_i32(x: torch.Tensor, y: torch.Tensor | None = None, *, exclusive: bool = False,
+                 total_out: torch.Tensor | None = None, block_threads: int = 0,
+                 workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """int32 prefix sum modulo 2^32 (see det.h); y may be x; returns y."""
+    _dev(x, "x")
+    if x.dtype != torch.int32 or (y is not None and y.dtype != torch.int32):
+        raise TypeError("det_scan_i32 takes int32 tensors")
+    if total_out is not None and (total_out.dtype != torch.int32 or total_out.numel() < 1):
+        raise TypeError("total_out must hold one int32")
+    if y is None:
+        y = torch.empty_like(x)
+    n = x.numel()
+    ws = _ws(workspace, lib().det_scan_i32_workspace_bytes(n), x.device)
+    _check(lib().det_scan_i32(_ptr(x), _ptr(y), n, SCAN_EXCLUSIVE if exclusive else SCAN_INCLUSIVE, _ptr(total_out),
+                              _ptr(ws), ws.numel(), block_threads, _stream(stream)), "det_scan_i32")
+    return y
+
+
+def det_slot_alloc(counter: torch.Tensor, index: torch.Tensor, *, count: torch.Tensor | None = None,
+                   slot_out: torch.Tensor | None = None, index_offset: int = 0, block_threads: int = 0,
+                   workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """slot = atomic_add(counter, index[i], count[i]) in thread order (see det.h); returns the slots."""
+    _dev(counter, "counter"), _dev(index, "index")
+    if counter.dtype != torch.int32 or index.dtype != torch.int32 or (count is not None and count.dtype != torch.int32):
+        raise TypeError("det_slot_alloc takes int32 tensors")
+    n = index.numel()
+    if count is not None and count.numel() != n:
+        raise ValueError("count must have one entry per record")
+    if slot_out is None:
+        slot_out = torch.empty(n, dtype=torch.int32, device=index.device)
+    ws = _ws(workspace, lib().det_slot_alloc_workspace_bytes(n, counter.numel()), index.device)
+    _check(lib().det_slot_alloc(_ptr(counter), counter.numel(), _ptr(index), int(index_offset), _ptr(count), n,
+                                _ptr(slot_out), _ptr(ws), ws.numel(), block_threads, _stream(stream)),
+           "det_slot_alloc")
+    return slot_out
 
 
 def det_scatter_add_rows(dst: torch.Tensor, idx: torch.Tensor, src: torch.Tensor, *, row_offset: int = 0,

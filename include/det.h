@@ -145,6 +145,45 @@ int det_scatter_add(void* out, int64_t out_len, const int32_t* bins, const void*
                     void* workspace, size_t workspace_bytes, int block_threads, void* stream);
 
 /* ------------------------------------------------------------------------
+ * det_scatter_sub -- the deterministic form of wp.atomic_sub(out, bins[i],
+ * values[i]): the values are negated and added in det_scatter_add's order,
+ * out[b] = out[b] + PT(-values of group b).  The leaves are negated (not the
+ * group's sum), so an exact zero from cancellation is +0.0 as the pages'
+ * "negated and added" gives.  Arguments, outputs, limits, workspace
+ * (det_scatter_add_workspace_bytes) and errors as det_scatter_add.
+ * Follows: Warp user guide "Deterministic Execution", "Pattern 1:
+ * Accumulation" (table row atomic_sub).
+ */
+int det_scatter_sub(void* out, int64_t out_len, const int32_t* bins, const void* values,
+                    int64_t n, int dtype, int32_t* perm_out, int32_t* seg_offsets_out,
+                    void* workspace, size_t workspace_bytes, int block_threads, void* stream);
+
+/* ------------------------------------------------------------------------
+ * det_scatter_min / det_scatter_max -- the deterministic form of
+ * wp.atomic_min / wp.atomic_max(out, bins[i], values[i]): for every bin b
+ * that receives at least one valid record, out[b] = op(out[b], op over the
+ * group), op = IEEE 754-2019 minimum / maximum (a NaN operand gives NaN, -0
+ * orders below +0).  That op is associative and commutative, so the result
+ * does not depend on any order; the kernels combine exact integer keys with
+ * integer atomics.  Bins without valid records are not touched (their bits,
+ * NaN payloads included, stay).  NaN results are the canonical quiet NaN.
+ *   out     device, out_len elements of dtype (read and written)
+ *   bins    device, n int32 (outside [0, out_len): skipped)
+ *   values  device, n elements of dtype
+ * Workspace: det_scatter_minmax_workspace_bytes(out_len, dtype) bytes.
+ * Limits and errors as det_scatter_add.  block_threads 128 gives 128-thread
+ * CTAs, any other value 256.
+ * Follows: Warp user guide "Deterministic Execution", "Pattern 1:
+ * Accumulation" (table rows atomic_min, atomic_max: values are grouped by
+ * destination and minimized / maximized).
+ */
+size_t det_scatter_minmax_workspace_bytes(int64_t out_len, int dtype);
+int det_scatter_min(void* out, int64_t out_len, const int32_t* bins, const void* values, int64_t n,
+                    int dtype, void* workspace, size_t workspace_bytes, int block_threads, void* stream);
+int det_scatter_max(void* out, int64_t out_len, const int32_t* bins, const void* values, int64_t n,
+                    int dtype, void* workspace, size_t workspace_bytes, int block_threads, void* stream);
+
+/* ------------------------------------------------------------------------
  * det_scatter_add_rows -- the tile row scatter of tile_atomic_add_indexed
  * along axis 0, deterministic: source row s (row_len elements) is added to
  * destination row r = idx[s] + row_offset when 0 <= r < dst_rows (else it
@@ -209,6 +248,52 @@ size_t det_segmented_scan_workspace_bytes(int64_t n, int64_t num_segments, int d
 int det_segmented_scan(const void* x, void* y, int64_t n, const int64_t* seg_offsets,
                        int64_t num_segments, int dtype, int flags, void* workspace,
                        size_t workspace_bytes, int block_threads, void* stream);
+
+/* ------------------------------------------------------------------------
+ * det_scan_i32 -- int32 prefix sum, inclusive (flags 0) or exclusive
+ * (flags DET_SCAN_EXCLUSIVE), modulo 2^32 (as int32 atomics wrap); every
+ * order of integer additions gives the same bits.  total_out (device, one
+ * int32, or NULL) receives the sum of all n values, so the page's "final
+ * count is offsets[n-1] + counts[n-1]" is available without a read-back.
+ *   x, y    device, n int32 (x == y allowed)
+ * Workspace: det_scan_i32_workspace_bytes(n).  Other flags give
+ * DET_ERR_INVALID_ARG.  The CTA size is fixed (block_threads is checked and
+ * otherwise ignored).
+ * Follows: Warp user guide "Deterministic Execution", "Picking the Right
+ * Mode" (count_positive -> array_scan(..., inclusive=False) ->
+ * write_positive) and "Pattern 2: Slot Allocation" (step 3).
+ */
+size_t det_scan_i32_workspace_bytes(int64_t n);
+int det_scan_i32(const int32_t* x, int32_t* y, int64_t n, int flags, int32_t* total_out,
+                 void* workspace, size_t workspace_bytes, int block_threads, void* stream);
+
+/* ------------------------------------------------------------------------
+ * det_slot_alloc -- the deterministic form of
+ *     slot = wp.atomic_add(counter, index[i], count[i])
+ * executed by threads i = 0 .. n-1: per counter element, reservations are
+ * served in thread order, so record i gets the element's value before the
+ * call plus the requests of the earlier records aimed at the same element,
+ * and every element then advances by its records' total.  Pre-existing
+ * nonzero counters and repeated (append-style) calls work.  Records whose
+ * element index[i] + index_offset is outside [0, num_counters) get slot -1
+ * and change nothing.  Arithmetic wraps modulo 2^32.
+ *   counter   device, num_counters int32 (read and written)
+ *   index     device, n int32
+ *   count     device, n int32 (slots requested; may be negative like an
+ *             atomic add's operand), or NULL for one slot each
+ *   slot_out  device, n int32
+ * Workspace: det_slot_alloc_workspace_bytes(n, num_counters).  Limits:
+ * n <= DET_MAX_RECORDS, num_counters <= 2^31 - 1.  slot_out must not
+ * overlap the inputs.
+ * Follows: Warp user guide "Deterministic Execution", "Pattern 2: Slot
+ * Allocation" (count, sort by counter element and thread order, segmented
+ * prefix scan, slots), "Pattern B: Slot Allocation Counters", and
+ * "Counter arrays are allocation counters".
+ */
+size_t det_slot_alloc_workspace_bytes(int64_t n, int64_t num_counters);
+int det_slot_alloc(int32_t* counter, int64_t num_counters, const int32_t* index, int64_t index_offset,
+                   const int32_t* count, int64_t n, int32_t* slot_out, void* workspace,
+                   size_t workspace_bytes, int block_threads, void* stream);
 
 /* ------------------------------------------------------------------------
  * Status.  det_read_status synchronizes `stream`, then copies the device

@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings(lib):
     from deterministic_floating_point_gb300 import det
     assert det.status_string(0) == "ok"
-    for code in range(1, 7):
+    for code in range(1, 8):
         assert det.status_string(code) != "unknown status"
 
 
@@ -63,3 +63,23 @@ def test_workspace_queries_are_host_only(lib):
     assert lib.det_scan_workspace_bytes(1 << 28, 0) > lib.det_scan_workspace_bytes(1 << 20, 0)
     assert lib.det_scatter_add_workspace_bytes(1 << 24, 1024, 0) > 4 * (1 << 24)
     assert lib.det_sum_workspace_bytes(-1, 0) == 0
+
+
+def test_host_checks_of_the_next_calls(lib):
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)
+    # det_scan_i32: unknown flag bits, null input, misaligned workspace
+    assert lib.det_scan_i32(fake, fake, 10, 2, None, fake, 1 << 20, 0, None) == 1
+    assert lib.det_scan_i32(None, fake, 10, 0, None, fake, 1 << 20, 0, None) == 1
+    assert lib.det_scan_i32(fake, fake, 10, 0, None, vp((1 << 20) + 8), 1 << 20, 0, None) == 4
+    # det_slot_alloc: null counter with counters, negative n, too many records
+    assert lib.det_slot_alloc(None, 4, fake, 0, None, 10, fake, fake, 1 << 20, 0, None) == 1
+    assert lib.det_slot_alloc(fake, 4, fake, 0, None, -1, fake, fake, 1 << 20, 0, None) == 1
+    assert lib.det_slot_alloc(fake, 4, fake, 0, None, 1 << 31, fake, fake, 1 << 40, 0, None) == 3
+    # det_scatter_min / max: dtype, small workspace
+    assert lib.det_scatter_min(fake, 4, fake, fake, 10, 9, fake, 1 << 20, 0, None) == 2
+    assert lib.det_scatter_max(fake, 1 << 20, fake, fake, 10, 0, fake, 64, 0, None) == 4
+    # det_scatter_sub shares det_scatter_add's checks
+    assert lib.det_scatter_sub(fake, 4, None, fake, 10, 0, None, None, fake, 1 << 20, 0, None) == 1
+    assert lib.det_scan_i32_workspace_bytes(1 << 20) > 0 and lib.det_slot_alloc_workspace_bytes(1 << 20, 4) > 0
+    assert lib.det_scatter_minmax_workspace_bytes(1000, 1) >= 8000

@@ -39,6 +39,14 @@ def test_sub_sign_and_untouched():
     assert np.array_equal(_bits(got[1:]), _bits(out0[1:]))   # bins without records keep their bits (-0.0 too)
 
 
+def test_sub_negates_values_not_the_group_result():
+    # (-1) + 1 is +0.0 while -(1 + (-1)) is -0.0: with old = -0.0 the two
+    # readings differ, and the pages negate the values
+    got = oracle.det_scatter_sub(np.array([-0.0], np.float32), np.array([0, 0], np.int32),
+                                 np.array([1.0, -1.0], np.float32))
+    assert got[0] == 0.0 and not np.signbit(got[0])
+
+
 @pytest.mark.parametrize("dtype", [np.float32, np.float64])
 def test_sub_equals_add_of_negated(dtype):
     # the pages define atomic_sub as "negated and added": same groups, same order
