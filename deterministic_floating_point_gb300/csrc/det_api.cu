@@ -1,5 +1,11 @@
 // Status reporting and measurement hooks for the C ABI.
 #include "det_common.cuh"
+
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <utility>
 #include "../../include/det_profile.h"
 
 namespace {
@@ -15,6 +21,55 @@ unsigned long long g_launches = 0;
 }  // namespace
 
 namespace det {
+namespace {
+constexpr int kAttrDevices = 64;
+std::atomic<int> g_sms[kAttrDevices];
+std::atomic<int> g_smem[kAttrDevices];
+std::mutex g_dyn_mu;
+std::map<std::pair<const void*, int>, size_t> g_dyn;
+
+int cached_attr(std::atomic<int>* cache, cudaDeviceAttr attr) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int v = (dev >= 0 && dev < kAttrDevices) ? cache[dev].load(std::memory_order_relaxed) : 0;
+  if (v == 0) {
+    cudaDeviceGetAttribute(&v, attr, dev);
+    if (dev >= 0 && dev < kAttrDevices && v > 0) cache[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+}  // namespace
+
+int device_sm_count() { return cached_attr(g_sms, cudaDevAttrMultiProcessorCount); }
+int device_max_smem_optin() { return cached_attr(g_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin); }
+
+cudaError_t ensure_dyn_smem(const void* kernel, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;   // within the default limit
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lk(g_dyn_mu);
+  size_t& cur = g_dyn[{kernel, dev}];
+  if (bytes <= cur) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) cur = bytes;
+  return e;
+}
+
+int kernel_occupancy(const void* kernel, int threads, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int, size_t>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_tuple(kernel, dev, threads, smem);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess) return -1;
+  cache[key] = per_sm;
+  return per_sm;
+}
+
 void launch_begin(const char* name, cudaStream_t s) {
   ++g_launches;
   if (g_prof.events && g_prof.count < g_prof.capacity && g_prof.count < 4096) {

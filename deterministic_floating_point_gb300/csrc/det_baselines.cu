@@ -43,6 +43,15 @@ __global__ void atomic_scatter_kernel(T* out, long long m, const int32_t* __rest
   }
 }
 
+__global__ void atomic_slot_kernel(int32_t* counter, long long C, const int32_t* __restrict__ index, long long off,
+                                   const int32_t* __restrict__ count, long long n, int32_t* __restrict__ slot_out) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const long long c = (long long)index[i] + off;
+    slot_out[i] = (c >= 0 && c < C) ? atomicAdd(counter + c, count ? count[i] : 1) : -1;
+  }
+}
+
 template <typename T>
 __global__ void atomic_rows_kernel(T* dst, long long R, long long W, const int32_t* __restrict__ idx, long long off,
                                    const T* __restrict__ src, long long M, T* prev) {
@@ -276,6 +285,19 @@ extern "C" int det_dlb_scan(const void* x, void* y, int64_t n, int dtype, void* 
     dlb_scan_kernel<double><<<(unsigned)nch, kDlbThreads, 0, s>>>(
         (const double*)x, (double*)y, n, (unsigned long long*)(w + kHeaderBytes),
         (unsigned long long*)(w + kHeaderBytes + arr), &h->ticket, &h->status);
+  launch_end(s);
+  return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
+}
+
+extern "C" int det_atomic_slot_alloc(int32_t* counter, int64_t num_counters, const int32_t* index, int64_t index_offset,
+                                     const int32_t* count, int64_t n, int32_t* slot_out, void* stream) {
+  if (n < 0 || num_counters < 0 || (num_counters > 0 && !counter) || (n > 0 && (!index || !slot_out)))
+    return DET_ERR_INVALID_ARG;
+  if (n == 0) return DET_OK;
+  cudaStream_t s = as_stream(stream);
+  const unsigned g = (unsigned)min((long long)((n + 255) / 256), 16LL * 152);
+  launch_begin("det_atomic_slot_alloc", s);
+  atomic_slot_kernel<<<g, 256, 0, s>>>(counter, num_counters, index, index_offset, count, n, slot_out);
   launch_end(s);
   return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
 }

@@ -244,6 +244,16 @@ inline int elem_size(int dtype) { return dtype == DET_F32 ? 4 : 8; }
 inline bool valid_dtype(int dtype) { return dtype == DET_F32 || dtype == DET_F64; }
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Attributes of the current device, queried once per device and cached.
+int device_sm_count();
+int device_max_smem_optin();
+// Raise `kernel`'s dynamic shared-memory limit to at least `bytes` on the
+// current device; the attribute is set once per kernel and device.
+cudaError_t ensure_dyn_smem(const void* kernel, size_t bytes);
+// Resident CTAs per SM of `kernel` at this CTA size and dynamic shared
+// memory, cached per kernel and device; -1 if the query failed.
+int kernel_occupancy(const void* kernel, int threads, size_t smem);
+
 // Launch bookkeeping for the measurement hooks of det_profile.h.  Every
 // kernel launch of the library goes through launch_begin / launch_end.
 void launch_begin(const char* name, cudaStream_t s);

@@ -96,8 +96,12 @@ __device__ __forceinline__ void apply(typename KeyOf<T>::U* keys, long long b, b
   }
 }
 
-// Records [0, n) in grid-stride order; m <= kSmemBins keeps the bins' keys in
-// shared memory per CTA and folds them into the global keys at the end.
+// Each lane takes 16 consecutive records per step (16-byte loads, all in
+// flight before any is combined; the order of combination is free), and the
+// warp combines them in 16 warp-wide rounds.  m <= kSmemBins keeps the bins'
+// keys in shared memory per CTA and folds them into the global keys at the end.
+constexpr int kPerLane = 16;
+
 template <typename T, bool MAX, bool SMEM>
 __global__ void __launch_bounds__(256)
 minmax_scatter_kernel(const int32_t* __restrict__ bins, const T* __restrict__ values, long long n, long long m,
@@ -110,19 +114,48 @@ minmax_scatter_kernel(const int32_t* __restrict__ bins, const T* __restrict__ va
     __syncthreads();
   }
   U* keys = SMEM ? skeys : gkeys;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  // whole warps step together (the group step needs every lane)
-  const long long first = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31);
-  for (long long base = first; base < n; base += stride) {
-    const long long i = base + (threadIdx.x & 31);
-    long long b = -1;
-    T v = T(0);
-    if (i < n) {
-      b = __ldg(bins + i);
-      v = __ldg(values + i);
+  const int lane = threadIdx.x & 31;
+  const long long wchunk = 32LL * kPerLane;
+  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  for (long long base = wid * wchunk; base < n; base += nwarps * wchunk) {   // whole warps step together
+    const long long i0 = base + (long long)lane * kPerLane;
+    int32_t bb[kPerLane];
+    T vv[kPerLane];
+    if (i0 + kPerLane <= n && (reinterpret_cast<uintptr_t>(bins + i0) & 15) == 0 &&
+        (reinterpret_cast<uintptr_t>(values + i0) & 15) == 0) {
+#pragma unroll
+      for (int q = 0; q < kPerLane / 4; ++q) {
+        const int4 w = __ldg(reinterpret_cast<const int4*>(bins + i0) + q);
+        bb[4 * q] = w.x, bb[4 * q + 1] = w.y, bb[4 * q + 2] = w.z, bb[4 * q + 3] = w.w;
+      }
+      if constexpr (sizeof(T) == 4) {
+#pragma unroll
+        for (int q = 0; q < kPerLane / 4; ++q) {
+          const float4 w = __ldg(reinterpret_cast<const float4*>(values + i0) + q);
+          vv[4 * q] = w.x, vv[4 * q + 1] = w.y, vv[4 * q + 2] = w.z, vv[4 * q + 3] = w.w;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < kPerLane / 2; ++q) {
+          const double2 w = __ldg(reinterpret_cast<const double2*>(values + i0) + q);
+          vv[2 * q] = w.x, vv[2 * q + 1] = w.y;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < kPerLane; ++e) {
+        const bool in = i0 + e < n;
+        bb[e] = in ? __ldg(bins + i0 + e) : -1;
+        vv[e] = in ? __ldg(values + i0 + e) : T(0);
+      }
     }
-    const bool valid = b >= 0 && b < m;
-    apply<T, MAX>(keys, valid ? b : -1, valid, to_key<T, MAX>(v));
+#pragma unroll
+    for (int e = 0; e < kPerLane; ++e) {
+      const long long b = bb[e];
+      const bool valid = b >= 0 && b < m;
+      apply<T, MAX>(keys, valid ? b : -1, valid, to_key<T, MAX>(vv[e]));
+    }
   }
   if (SMEM) {
     __syncthreads();
@@ -150,17 +183,14 @@ int minmax_impl(T* out, long long m, const int32_t* bins, const T* values, long 
   if (cudaMemsetAsync(ws, 0, kHeaderBytes, s) != cudaSuccess) return DET_ERR_CUDA;
   if (m == 0) return DET_OK;
   if (cudaMemsetAsync(gkeys, MAX ? 0x00 : 0xff, (size_t)m * sizeof(U), s) != cudaSuccess) return DET_ERR_CUDA;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = device_sm_count();
   const int threads = bt == 128 ? 128 : 256;   // the kernel is built for at most 256 threads
   if (n > 0) {
     const bool smem = m <= kSmemBins;
-    const long long want = (n + (long long)threads * 16 - 1) / ((long long)threads * 16);   // >= 16 records per thread
+    const long long want = (n + (long long)threads * 64 - 1) / ((long long)threads * 64);   // >= 64 records per thread
     const long long grid = std::max(1LL, std::min(want, 4LL * std::max(sms, 1)));
     const size_t sb = smem ? (size_t)m * sizeof(U) : 0;   // up to 64 KB: above the default 48 KB for f64
-    if (smem && cudaFuncSetAttribute(minmax_scatter_kernel<T, MAX, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)std::max<size_t>(sb, 1)) != cudaSuccess)
+    if (smem && ensure_dyn_smem((const void*)minmax_scatter_kernel<T, MAX, true>, sb) != cudaSuccess)
       return DET_ERR_CUDA;
     launch_begin("det_minmax_scatter", s);
     if (smem)

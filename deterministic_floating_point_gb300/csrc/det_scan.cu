@@ -874,14 +874,12 @@ static cudaError_t launch_scan(const ScanArgs<T>& a, int threads, cudaStream_t s
     // persistent: one CTA per SM (cooperative launch), chunks assigned round-robin
     const size_t smem = ScanGeom<T>::kStageBytes + sizeof(KeepSmem<T>);
     auto kern = scan_keep_kernel<T, SEG, REV, EXCL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_dyn_smem((const void*)kern, smem);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return cudaErrorUnknown;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 1024, smem);
-    if (e != cudaSuccess) return e;
+    const int sms = device_sm_count();
+    if (sms <= 0) return cudaErrorUnknown;
+    const int per_sm = kernel_occupancy((const void*)kern, 1024, smem);
+    if (per_sm < 0) return cudaErrorUnknown;
     const long long grid = min((long long)sms * per_sm, a.nchunks + 1);
     if (grid >= 2) {
       void* args[] = {const_cast<ScanArgs<T>*>(&a)};
@@ -895,7 +893,7 @@ static cudaError_t launch_scan(const ScanArgs<T>& a, int threads, cudaStream_t s
   }
   const size_t smem = ScanGeom<T>::kStageBytes + sizeof(ScanSmem<T>);
   auto kern = scan_kernel<T, SEG, REV, EXCL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dyn_smem((const void*)kern, smem);
   if (e != cudaSuccess) return e;
   launch_begin(SEG ? "det_segmented_scan" : "det_scan", s);
   kern<<<(unsigned)(a.nchunks + 1), threads, smem, s>>>(a);

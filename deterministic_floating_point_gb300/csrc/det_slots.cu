@@ -64,6 +64,86 @@ __global__ void counter_kernel(const int32_t* __restrict__ seg, long long C, con
   counter[b] = (int32_t)((unsigned)counter[b] + add);
 }
 
+// One counter element: no sort is needed -- in thread order, every record's
+// slot is the counter plus the requests of the records before it.
+struct RequestSrc {
+  const int32_t* index;
+  const int32_t* count;
+  long long off;
+  __device__ __forceinline__ void load(long long i0, long long n, unsigned (&v)[kIScanPer]) const {
+    int32_t ix[kIScanPer], cn[kIScanPer];
+    const bool vec = i0 + kIScanPer <= n && (reinterpret_cast<uintptr_t>(index + i0) & 15) == 0 &&
+                     (!count || (reinterpret_cast<uintptr_t>(count + i0) & 15) == 0);
+    if (vec) {
+#pragma unroll
+      for (int q = 0; q < kIScanPer / 4; ++q) {
+        const int4 w = __ldg(reinterpret_cast<const int4*>(index + i0) + q);
+        ix[4 * q] = w.x, ix[4 * q + 1] = w.y, ix[4 * q + 2] = w.z, ix[4 * q + 3] = w.w;
+        if (count) {
+          const int4 c = __ldg(reinterpret_cast<const int4*>(count + i0) + q);
+          cn[4 * q] = c.x, cn[4 * q + 1] = c.y, cn[4 * q + 2] = c.z, cn[4 * q + 3] = c.w;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < kIScanPer; ++e) {
+        const bool in = i0 + e < n;
+        ix[e] = in ? __ldg(index + i0 + e) : -1;
+        cn[e] = (in && count) ? __ldg(count + i0 + e) : 0;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < kIScanPer; ++e) {
+      const bool valid = i0 + e < n && (long long)ix[e] + off == 0;
+      v[e] = valid ? (count ? (unsigned)cn[e] : 1u) : 0u;
+    }
+  }
+};
+
+struct SlotDst {
+  const int32_t* index;
+  long long off;
+  const int32_t* counter;
+  int32_t* slot_out;
+  __device__ __forceinline__ void store(long long i0, long long n, const unsigned (&ex)[kIScanPer],
+                                        const unsigned (&)[kIScanPer]) const {
+    const unsigned c0 = (unsigned)*counter;   // advanced only by a later kernel
+#pragma unroll
+    for (int e = 0; e < kIScanPer; ++e) {
+      const long long i = i0 + e;
+      if (i >= n) break;
+      const bool valid = (long long)__ldg(index + i) + off == 0;
+      slot_out[i] = valid ? (int32_t)(c0 + ex[e]) : -1;
+    }
+  }
+};
+
+__global__ void advance_counter_kernel(int32_t* __restrict__ counter, const int32_t* __restrict__ total) {
+  *counter = (int32_t)((unsigned)*counter + (unsigned)*total);
+}
+
+// One slot each and a one-pass sort: in input order, slot_out[i] =
+// counter[b] + (sorted position of i - start of b's group), b = index[i] +
+// offset; the sort wrote the positions in input order.
+template <bool SMEM>
+__global__ void __launch_bounds__(256)
+slot_rank_kernel(const int32_t* __restrict__ seg, long long C, const int32_t* __restrict__ index, long long off,
+                 const int32_t* __restrict__ rank, const int32_t* __restrict__ counter, long long n,
+                 int32_t* __restrict__ slot_out) {
+  extern __shared__ int32_t sseg[];
+  if (SMEM) {
+    for (long long i = threadIdx.x; i <= C; i += blockDim.x) sseg[i] = seg[i];
+    __syncthreads();
+  }
+  const int32_t* sg = SMEM ? sseg : seg;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const long long b = (long long)__ldg(index + i) + off;
+    int32_t slot = -1;
+    if (b >= 0 && b < C) slot = (int32_t)((unsigned)counter[b] + (unsigned)(__ldg(rank + i) - sg[b]));
+    slot_out[i] = slot;
+  }
+}
+
 struct SlotLayout {
   SortPlan plan;
   size_t excl = 0, iscan = 0, total = 0;
@@ -104,6 +184,46 @@ extern "C" int det_slot_alloc(int32_t* counter, int64_t num_counters, const int3
   const SlotLayout L = slot_layout(n, C, count != nullptr, block_threads);
   if (workspace_bytes < L.total) return DET_ERR_WORKSPACE;
   char* w = reinterpret_cast<char*>(workspace);
+  if (C == 1 && n > 0) {
+    // one counter element: an exclusive scan of the requests, no sort
+    if (cudaMemsetAsync(workspace, 0, kHeaderBytes, s) != cudaSuccess) return DET_ERR_CUDA;
+    int32_t* total = reinterpret_cast<int32_t*>(w + L.excl);
+    unsigned* tsum = reinterpret_cast<unsigned*>(w + L.iscan);
+    int rc = enqueue_iscan(RequestSrc{index, count, index_offset}, SlotDst{index, index_offset, counter, slot_out},
+                           n, total, tsum, s);
+    if (rc != DET_OK) return rc;
+    launch_begin("det_slot_counters", s);
+    advance_counter_kernel<<<1, 1, 0, s>>>(counter, total);
+    launch_end(s);
+    return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
+  }
+  const int sms = device_sm_count();
+  const long long grid = std::max(1LL, std::min((long long)((n + 255) / 256), 8LL * std::max(sms, 1)));
+  const bool smem = C + 1 <= kSmemSeg;
+  const size_t sb = smem ? (size_t)(C + 1) * 4 : 0;
+  if (!count && n > 0 && C > 0) {
+    const SortPlan rp = make_sort_plan(n, C, 0, false, block_threads);
+    if (rp.passes == 1 && rp.total <= L.excl) {
+      // one slot each, one sort pass: the pass writes every record's sorted
+      // position in input order, and the slots follow in input order too
+      int32_t* rank = reinterpret_cast<int32_t*>(w + L.excl);
+      int fb = 0;
+      int rc = enqueue_sort(rp, workspace, index, index_offset, nullptr, nullptr, s, &fb, rank);
+      if (rc != DET_OK) return rc;
+      const int32_t* seg = reinterpret_cast<const int32_t*>(w + rp.seg);
+      launch_begin("det_slot_alloc", s);
+      if (smem)
+        slot_rank_kernel<true><<<(unsigned)grid, 256, sb, s>>>(seg, C, index, index_offset, rank, counter, n, slot_out);
+      else
+        slot_rank_kernel<false><<<(unsigned)grid, 256, 0, s>>>(seg, C, index, index_offset, rank, counter, n,
+                                                               slot_out);
+      launch_end(s);
+      launch_begin("det_slot_counters", s);
+      counter_kernel<false><<<(unsigned)((C + 255) / 256), 256, 0, s>>>(seg, C, nullptr, counter);
+      launch_end(s);
+      return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
+    }
+  }
   // skipped records keep slot -1
   if (n > 0 && cudaMemsetAsync(slot_out, 0xff, (size_t)n * 4, s) != cudaSuccess) return DET_ERR_CUDA;
   if (n == 0 || C == 0) return cudaMemsetAsync(workspace, 0, kHeaderBytes, s) == cudaSuccess ? DET_OK : DET_ERR_CUDA;
@@ -122,12 +242,6 @@ extern "C" int det_slot_alloc(int32_t* counter, int64_t num_counters, const int3
                           reinterpret_cast<int32_t*>(excl + n), w + L.iscan, s);
     if (rc != DET_OK) return rc;
   }
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long grid = std::max(1LL, std::min((long long)((n + 255) / 256), 8LL * std::max(sms, 1)));
-  const bool smem = C + 1 <= kSmemSeg;
-  const size_t sb = smem ? (size_t)(C + 1) * 4 : 0;
   launch_begin("det_slot_alloc", s);
   if (count) {
     if (smem)

@@ -44,6 +44,7 @@ struct PassArgs {
   unsigned int* status;
   unsigned int* n_valid;
   int32_t* seg_out;            // one-pass sorts: segment starts (m + 1), written by CTA 0 of the pass
+  int32_t* rank_out;           // one-pass sorts: sorted position of every valid record, in input order
 };
 
 // Digit of record i of a pass, or 0xffffffff if it is past the end or
@@ -441,6 +442,18 @@ __global__ void __launch_bounds__(256, 3) sort_pass_kernel(PassArgs a) {
     const unsigned d = pk >> 16;
     packed[r] = (d << 16) | (lstart[d] + wcnt[warp * ndig + d] + (pk & 0xffffu));
   }
+  if (a.rank_out) {
+    // only each record's sorted position is wanted: write it in input order
+    // (coalesced) and move nothing
+#pragma unroll
+    for (int r = 0; r < kIPT; ++r) {
+      const unsigned pk = packed[r];
+      if (pk == 0xffffffffu) continue;
+      const unsigned d = pk >> 16;
+      a.rank_out[wbase + (long long)r * 32 + lane] = (int32_t)(gbase[d] - lstart[d] + (pk & 0xffffu));
+    }
+    return;
+  }
   __syncthreads();   // the peer-mask and counter words are free from here on
 
   // ---- one-pass sorts of full, aligned tiles whose digit runs are long (16
@@ -758,9 +771,7 @@ template <int VB>
 static cudaError_t launch_pass(const PassArgs& a, bool first, bool idx, bool keys_out, int threads, long long tiles,
                                cudaStream_t s) {
   const int ndig = 1 << a.D;
-  int dev = 0, max_smem = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  const int max_smem = device_max_smem_optin();
   const size_t tail = (size_t)3 * (ndig + 1) * 4;
   const bool stage = pass_front_bytes(threads / 32, ndig, a.K, VB, idx, keys_out, true) + tail <= (size_t)max_smem;
   const size_t smem = pass_front_bytes(threads / 32, ndig, a.K, VB, idx, keys_out, stage) + tail;
@@ -771,7 +782,7 @@ static cudaError_t launch_pass(const PassArgs& a, bool first, bool idx, bool key
   DET_PICK(true, true, true) DET_PICK(true, true, false) DET_PICK(true, false, true) DET_PICK(true, false, false)
   DET_PICK(false, true, true) DET_PICK(false, true, false) DET_PICK(false, false, true) DET_PICK(false, false, false)
 #undef DET_PICK
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dyn_smem((const void*)k, smem);
   if (e != cudaSuccess) return e;
   launch_begin("det_sort_pass", s);
   k<<<(unsigned)tiles, threads, smem, s>>>(a);
@@ -780,7 +791,7 @@ static cudaError_t launch_pass(const PassArgs& a, bool first, bool idx, bool key
 }
 
 int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key_offset, const void* values,
-                 int32_t* perm_out, cudaStream_t s, int* final_buf) {
+                 int32_t* perm_out, cudaStream_t s, int* final_buf, int32_t* rank_out) {
   char* w = reinterpret_cast<char*>(ws);
   SortHdr* h = reinterpret_cast<SortHdr*>(ws);
   if (cudaMemsetAsync(w, 0, kHeaderBytes, s) != cudaSuccess) return DET_ERR_CUDA;
@@ -815,6 +826,7 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
     a.status = &h->status;
     a.n_valid = &h->n_valid;
     a.seg_out = p.passes == 1 ? seg : nullptr;
+    a.rank_out = p.passes == 1 ? rank_out : nullptr;
     const size_t csmem = (size_t)ndig * 4;
     const long long K = (long long)p.threads * kIPT;
     launch_begin("det_sort_count", s);

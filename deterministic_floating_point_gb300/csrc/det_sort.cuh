@@ -47,9 +47,11 @@ SortPlan make_sort_plan(long long n, long long m, int value_bytes, bool need_idx
 // Enqueue the whole sort: histogram, digit starts, passes, segment starts.
 // Results: sorted values at plan.vals[final], sorted indices at
 // perm_out (if not null) else plan.idx[final], segment starts (m+1 int32)
-// at plan.seg.  Returns DET_OK or DET_ERR_CUDA.
+// at plan.seg.  With rank_out (one-pass plans without values or indices
+// only) the pass writes each valid record's sorted position to rank_out[i],
+// in input order, and moves nothing else.  Returns DET_OK or DET_ERR_CUDA.
 int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key_offset, const void* values,
-                 int32_t* perm_out, cudaStream_t s, int* final_buf);
+                 int32_t* perm_out, cudaStream_t s, int* final_buf, int32_t* rank_out = nullptr);
 
 // Segmented pairwise tree: out[b] = out[b] + PT(vals[seg[b] .. seg[b+1]))
 // for every non-empty b.  T is float or double.

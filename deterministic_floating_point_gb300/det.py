@@ -57,6 +57,7 @@ _SIGNATURES = {
     "det_atomic_sum": (_int, [_vp, _i64, _int, _vp, _vp]),
     "det_atomic_scatter_add": (_int, [_vp, _i64, _vp, _vp, _i64, _int, _vp]),
     "det_atomic_scatter_add_rows": (_int, [_vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _int, _vp]),
+    "det_atomic_slot_alloc": (_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp]),
     "det_dlb_scan_workspace_bytes": (_sz, [_i64, _int]),
     "det_dlb_scan": (_int, [_vp, _vp, _i64, _int, _vp, _sz, _vp]),
 }
@@ -71,6 +72,8 @@ class DetError(RuntimeError):
 def lib():
     """The loaded ``libdet.so``; raises if it has not been built."""
     global _lib
+    if _lib is not None:   # loaded: no lock on the per-call path
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
@@ -391,3 +394,11 @@ def dlb_scan(x: torch.Tensor, y: torch.Tensor, workspace: torch.Tensor | None = 
     _check(lib().det_dlb_scan(_ptr(x), _ptr(y), x.numel(), _code(x), _ptr(ws), ws.numel(), _stream(stream)),
            "det_dlb_scan")
     return y
+
+
+def atomic_slot_alloc(counter: torch.Tensor, index: torch.Tensor, slot_out: torch.Tensor, *,
+                      count: torch.Tensor | None = None, index_offset: int = 0, stream=None) -> torch.Tensor:
+    """Baseline: slot = atomicAdd(counter[index[i]], ...) in arrival order (see det_baselines.h)."""
+    _check(lib().det_atomic_slot_alloc(_ptr(counter), counter.numel(), _ptr(index), int(index_offset), _ptr(count),
+                                       index.numel(), _ptr(slot_out), _stream(stream)), "det_atomic_slot_alloc")
+    return slot_out

@@ -35,6 +35,14 @@ int det_atomic_scatter_add_rows(void* dst, int64_t dst_rows, int64_t row_len, co
                                 int64_t row_offset, const void* src, int64_t src_rows, void* prev_out, int dtype,
                                 void* stream);
 
+/* slot_out[i] = atomicAdd(&counter[index[i] + index_offset], count[i] or 1)
+ * with integer atomics in arrival order (-1 for indices outside the
+ * counters): the slot-allocation pattern of Warp user guide "Deterministic
+ * Execution", "Pattern 2: Slot Allocation", as it runs without deterministic
+ * mode.  The counters' final values are deterministic, the slots are not. */
+int det_atomic_slot_alloc(int32_t* counter, int64_t num_counters, const int32_t* index, int64_t index_offset,
+                          const int32_t* count, int64_t n, int32_t* slot_out, void* stream);
+
 /* Inclusive forward prefix sum by the unmodified decoupled look-back: each
  * chunk publishes its aggregate (PARTIAL) and then its inclusive prefix
  * (INCLUSIVE); the look-back adds predecessors' values until it meets an
