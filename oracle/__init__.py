@@ -58,6 +58,7 @@ def _load():
                 getattr(lib, f"oracle_scan_{sfx}").argtypes = [vp, vp, i64, ctypes.c_int, vp]
                 getattr(lib, f"oracle_segmented_scan_{sfx}").argtypes = [vp, vp, i64, vp, i64, ctypes.c_int]
                 getattr(lib, f"oracle_scatter_sub_{sfx}").argtypes = [vp, i64, vp, vp, i64]
+                getattr(lib, f"oracle_scatter_add_rows_ordered_{sfx}").argtypes = [vp, i64, i64, vp, i64, vp, i64, vp]
                 getattr(lib, f"oracle_scatter_minmax_{sfx}").argtypes = [vp, i64, vp, vp, i64, ctypes.c_int]
             lib.oracle_scan_i32.argtypes = [vp, vp, i64, ctypes.c_int, vp]
             lib.oracle_slot_alloc.argtypes = [vp, i64, vp, i64, vp, i64, vp]
@@ -216,3 +217,20 @@ def det_slot_alloc(counter: np.ndarray, index: np.ndarray, count: np.ndarray | N
     _check(_load().oracle_slot_alloc(_ptr(ctr), ctr.size, _ptr(index), int(index_offset), _ptr(cnt), index.size,
                                      _ptr(slots)), "slot_alloc")
     return slots, ctr
+
+
+def det_scatter_add_rows_ordered(dst: np.ndarray, idx: np.ndarray, src: np.ndarray, row_offset: int = 0):
+    """Row scatter applied one source row at a time in ascending order; returns (new_dst, prev)."""
+    src = np.ascontiguousarray(src)
+    sfx = _sfx(src.dtype)
+    res = np.array(dst, dtype=src.dtype, copy=True, order="C")
+    if res.ndim != 2 or src.ndim != 2 or res.shape[1] != src.shape[1]:
+        raise ValueError("dst and src must be 2-D with equal row length")
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    if idx.size != src.shape[0]:
+        raise ValueError("idx must have one entry per source row")
+    prev = np.empty_like(src)
+    rc = getattr(_load(), f"oracle_scatter_add_rows_ordered_{sfx}")(
+        _ptr(res), res.shape[0], res.shape[1], _ptr(idx), int(row_offset), _ptr(src), src.shape[0], _ptr(prev))
+    _check(rc, "scatter_add_rows_ordered")
+    return res, prev

@@ -216,6 +216,37 @@ int FN(oracle_scatter_add_rows)(T* dst, int64_t dst_rows, int64_t row_len,
     return 0;
 }
 
+/* det_scatter_add_rows_ordered: the same row scatter with the tile page's
+ * "returns the previous value" read as atomics applied one source row at a
+ * time in ascending s: per destination row and column the contributions are
+ * added sequentially to the old value, prev_out[s] receives the running value
+ * just before row s is added, and the destination ends at the full
+ * sequential sum (Warp language reference "warp.tile_atomic_add_indexed",
+ * returns; the index-order running prefix per destination).  Skipped rows get
+ * prev +0.0 as in det_scatter_add_rows. */
+int FN(oracle_scatter_add_rows_ordered)(T* dst, int64_t dst_rows, int64_t row_len,
+                                        const int32_t* idx, int64_t row_offset,
+                                        const T* src, int64_t src_rows, T* prev_out)
+{
+    if (dst_rows < 0 || row_len < 0 || src_rows < 0) return 1;
+    if (src_rows > 0 && (!idx || (row_len > 0 && !src))) return 1;
+    if (dst_rows > 0 && row_len > 0 && !dst) return 1;
+    if (src_rows > 2147483647LL || dst_rows > 2147483647LL) return 2;
+    const int64_t R = dst_rows, W = row_len, M = src_rows;
+    for (int64_t s = 0; s < M; ++s) {          /* ascending source row: thread order */
+        const int64_t r = (int64_t)idx[s] + row_offset;
+        for (int64_t j = 0; j < W; ++j) {
+            if (r < 0 || r >= R) {
+                if (prev_out) prev_out[s * W + j] = (T)0.0;
+                continue;
+            }
+            if (prev_out) prev_out[s * W + j] = dst[r * W + j];
+            dst[r * W + j] = dst[r * W + j] + src[s * W + j];
+        }
+    }
+    return 0;
+}
+
 /* ---------------------------------------------------------------------- */
 /* Anchored decoupled look-back scan (drjit-core pull request "Make CUDA
  * floating-point prefix sums deterministic", sections "Implementation" and

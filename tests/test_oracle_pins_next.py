@@ -1,5 +1,5 @@
-"""CPU pins of the oracle's scatter-sub, scatter-min/max, int32 scan and slot
-allocation against facts the pages and the mathematics fix, computed here
+"""CPU pins of the oracle's scatter-sub, scatter-min/max, int32 scan, slot
+allocation and the ordered row scatter against facts the pages and the mathematics fix, computed here
 without the oracle: integer-exact sums, numpy's grouped minimum/maximum, numpy
 cumulative sums with int32 wrap-around, the pages' compaction example
 (Warp "Deterministic Execution", "Pattern 2: Slot Allocation" and "Picking the
@@ -196,3 +196,47 @@ def test_slot_alloc_offset_and_empty():
     assert s.tolist() == [3, 9, 4, -1] and c.tolist() == [5, 10]
     s, c = oracle.det_slot_alloc(np.array([3], np.int32), np.zeros(0, np.int32))
     assert s.size == 0 and c.tolist() == [3]
+
+
+# ---------------------------------------------------------------------------
+# ordered row scatter: contributions applied one source row at a time
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+def test_rows_ordered_matches_numpy_add_at(dtype):
+    # numpy's unbuffered add.at applies repeated indices one by one in index order
+    rng = np.random.default_rng(31)
+    src = rng.standard_normal((3000, 5)).astype(dtype)
+    idx = rng.integers(-2, 42, 3000).astype(np.int32)
+    dst0 = rng.standard_normal((40, 5)).astype(dtype)
+    got, prev = oracle.det_scatter_add_rows_ordered(dst0, idx, src)
+    want = dst0.copy()
+    ok = (idx >= 0) & (idx < 40)
+    np.add.at(want, idx[ok], src[ok])
+    assert np.array_equal(_bits(got), _bits(want))
+    assert not prev[~ok].any()
+
+
+def test_rows_ordered_prev_is_the_running_prefix():
+    # integer-valued rows: prev of the k-th contributor of r is dst0[r] + the sum of the earlier ones
+    rng = np.random.default_rng(32)
+    src = rng.integers(-50, 50, (5000, 3)).astype(np.float32)
+    idx = rng.integers(0, 17, 5000).astype(np.int32)
+    dst0 = rng.integers(-100, 100, (17, 3)).astype(np.float32)
+    got, prev = oracle.det_scatter_add_rows_ordered(dst0, idx, src)
+    for r in range(17):
+        sel = np.flatnonzero(idx == r)
+        cs = np.cumsum(src[sel].astype(np.int64), axis=0)
+        assert np.array_equal(prev[sel], (dst0[r].astype(np.int64) + cs - src[sel].astype(np.int64)).astype(np.float32))
+        assert np.array_equal(got[r], (dst0[r].astype(np.int64) + cs[-1]).astype(np.float32))
+
+
+def test_rows_ordered_equals_default_for_distinct_rows():
+    # with every destination hit at most once both readings return the plain gather
+    rng = np.random.default_rng(33)
+    src = rng.standard_normal((64, 4)).astype(np.float32)
+    idx = rng.permutation(100)[:64].astype(np.int32)
+    dst0 = rng.standard_normal((100, 4)).astype(np.float32)
+    a = oracle.det_scatter_add_rows_ordered(dst0, idx, src)
+    b = oracle.det_scatter_add_rows(dst0, idx, src)
+    assert np.array_equal(_bits(a[0]), _bits(b[0])) and np.array_equal(_bits(a[1]), _bits(b[1]))
+    assert np.array_equal(a[1], dst0[idx])
