@@ -223,6 +223,42 @@ def build_workload(name, torch, det, dev):
                     config={"workload": f"det_scatter_{op} n={n} N(0,1) {dt}, {m} uniform bins, seed 2", "n": n,
                             "bins": m, "l2": "L2 flushed between timed steps"})
 
+    if name == "scatter_vec3":
+        values_np, bins_np, out0_np = workloads.vec_scatter_input(dtype=npdt)
+        n, W = values_np.shape
+        m = out0_np.shape[0]
+        v = torch.from_numpy(values_np).to(dev)
+        b = torch.from_numpy(bins_np).to(dev)
+        out = torch.from_numpy(out0_np).to(dev)
+        s = values_np.itemsize
+        ws = det.workspace(det.lib().det_scatter_add_vec_workspace_bytes(n, m, W, code), dev)
+        host_v = torch.from_numpy(values_np).pin_memory()
+        host_b = torch.from_numpy(bins_np).pin_memory()
+        host_out = torch.empty_like(out, device="cpu").pin_memory()
+
+        def step():
+            det.det_scatter_add_vec(out, b, v, workspace=ws, block_threads=BLOCK_THREADS)
+
+        def e2e_step():
+            v.copy_(host_v, non_blocking=True)
+            b.copy_(host_b, non_blocking=True)
+            det.det_scatter_add_vec(out, b, v, workspace=ws)
+            host_out.copy_(out, non_blocking=True)
+
+        def oracle_sample():
+            import oracle
+            k = min(n, 1 << 21)
+            reps, secs = _timed_oracle(lambda: oracle.det_scatter_add_rows(out0_np, bins_np[:k], values_np[:k]))
+            return k * W * reps, secs, f"{reps} x vec{W} scatter of the first {k} records, 1 thread"
+
+        # sort (key in, index out), gather (index in, W components in and out), W trees (W components in)
+        step_bytes = n * (4 + 4 + 4 + 2 * W * s + W * s) + 2 * m * W * s
+        return dict(state={"out": out, "out0": torch.from_numpy(out0_np).to(dev), "b": b, "v": v}, step=step,
+                    elems=n * W, algo_bytes=n * (4 + 4), step_bytes=step_bytes, dominant="det_sort_pass",
+                    dtype=dt, e2e_step=e2e_step, h2d=n * (4 + W * s), d2h=m * W * s, oracle_sample=oracle_sample,
+                    config={"workload": f"det_scatter_add_vec n={n} vec{W} N(0,1) {dt}, {m} uniform bins, seed 6",
+                            "n": n, "width": W, "bins": m, "l2": "L2 flushed between timed steps"})
+
     if name == "scan_i32":
         n = N_OVERRIDE or workloads.SCAN_N
         # count -> exclusive scan -> write: 0/1 flags of the scan workload's values
@@ -343,6 +379,7 @@ def build_workload(name, torch, det, dev):
                             "l2": "L2 flushed between timed steps"})
 
     if name.startswith("rows"):
+        ordered = name.startswith("rows_ordered")
         src_np, idx_np, dst0_np = workloads.rows_input(dtype=npdt)
         M, W = src_np.shape
         R = dst0_np.shape[0]
@@ -357,28 +394,31 @@ def build_workload(name, torch, det, dev):
         host_prev = torch.empty_like(host_src).pin_memory()
 
         def step():
-            det.det_scatter_add_rows(dst, idx, src, prev_out=prev, workspace=ws, block_threads=BLOCK_THREADS)
+            det.det_scatter_add_rows(dst, idx, src, prev_out=prev, workspace=ws, block_threads=BLOCK_THREADS,
+                                     ordered=ordered)
 
         def e2e_step():
             src.copy_(host_src, non_blocking=True)
             idx.copy_(host_idx, non_blocking=True)
-            det.det_scatter_add_rows(dst, idx, src, prev_out=prev, workspace=ws)
+            det.det_scatter_add_rows(dst, idx, src, prev_out=prev, workspace=ws, ordered=ordered)
             host_prev.copy_(prev, non_blocking=True)
 
         def oracle_sample():
             import oracle
             k = 1 << 17
-            reps, secs = _timed_oracle(lambda: oracle.det_scatter_add_rows(dst0_np, idx_np[:k], src_np[:k]))
-            return k * W * reps, secs, f"{reps} x det_scatter_add_rows of the first {k} source rows, 1 thread"
+            f = oracle.det_scatter_add_rows_ordered if ordered else oracle.det_scatter_add_rows
+            reps, secs = _timed_oracle(lambda: f(dst0_np, idx_np[:k], src_np[:k]))
+            return k * W * reps, secs, f"{reps} x row scatter of the first {k} source rows, 1 thread"
 
         rows_bytes = 2 * M * W * s + 2 * R * W * s + 4 * M    # src in, prev out, dst in/out, sorted ids
         return dict(state={"dst": dst, "dst0": torch.from_numpy(dst0_np).to(dev), "idx": idx, "src": src,
                            "prev": prev}, step=step, elems=M * W, algo_bytes=rows_bytes,
                     step_bytes=rows_bytes + 12 * M,
-                    dominant="det_rows", dtype=dt, e2e_step=e2e_step, h2d=M * W * s + 4 * M, d2h=M * W * s,
-                    oracle_sample=oracle_sample,
-                    config={"workload": f"det_scatter_add_rows src {M}x{W} N(0,1) {dt}, rows uniform over {R}, "
-                                        "prev returned, seed 5", "src_rows": M, "dst_rows": R, "row_len": W,
+                    dominant="det_rows_ordered" if ordered else "det_rows", dtype=dt, e2e_step=e2e_step,
+                    h2d=M * W * s + 4 * M, d2h=M * W * s, oracle_sample=oracle_sample,
+                    config={"workload": f"det_scatter_add_rows{'_ordered' if ordered else ''} src {M}x{W} N(0,1) "
+                                        f"{dt}, rows uniform over {R}, prev returned, seed 5",
+                            "src_rows": M, "dst_rows": R, "row_len": W,
                             "l2": "inputs larger than L2; L2 flushed between timed steps"})
 
     raise SystemExit(f"unknown workload {name}")
@@ -497,6 +537,14 @@ def add_checks(name, wl, torch, det, dev):
         wl["det_once"], wl["base_once"] = d1, b1
         wl["base_step"] = lambda: det.atomic_slot_alloc(ctr, idx, bslots)
         wl["base_name"] = "atomic_slot_alloc (atomicAdd slots)"
+    elif name == "scatter_vec3":
+        out, out0 = st["out"], st["out0"]
+
+        def d1():
+            out.copy_(out0)
+            wl["step"]()
+            return fingerprint(torch, out)
+        wl["det_once"] = d1
     elif name.startswith("scatter") or name.startswith("skew"):
         out, out0, b, v = st["out"], st["out0"], st["b"], st["v"]
 
@@ -585,7 +633,7 @@ def traffic_for(kernel, workload):
 
 OPS = ["sum", "sum_f64", "sum_small", "scatter_f64", "scatter_bin0", "skew", "skew_f32", "scan", "scan_f64",
        "scan_small", "segscan", "rows", "scatter_sub", "scatter_min", "scatter_max", "scan_i32", "slot_alloc",
-       "slot_alloc_multi"]
+       "slot_alloc_multi", "scatter_vec3", "rows_ordered"]
 
 
 def measure_op(name, torch, det, dev, flush, steps, runs, peak):

@@ -75,6 +75,60 @@ rows_kernel(T* __restrict__ dst, long long R, long long W, const T* __restrict__
   }
 }
 
+// Ordered reading: per destination row and column the contributors are
+// added one at a time in ascending source row, each getting the running
+// value before its own add as prev (atomics applied in thread order).
+template <typename T>
+__global__ void __launch_bounds__(256)
+rows_ordered_kernel(T* __restrict__ dst, long long R, long long W, const T* __restrict__ src,
+                    const int32_t* __restrict__ perm, const int32_t* __restrict__ seg,
+                    const unsigned int* __restrict__ n_valid, T* __restrict__ prev, long long src_rows) {
+  const long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= R) return;
+  const long long N = *n_valid;
+  const long long hi = min((long long)seg[r + 1], N), lo = max(0LL, min((long long)seg[r], hi));
+  const long long L = hi - lo;
+  if (L <= 0) return;
+  for (long long c0 = 0; c0 < W; c0 += 32 * kCPL) {
+    long long col[kCPL];
+    bool cok[kCPL];
+    T acc[kCPL];
+#pragma unroll
+    for (int c = 0; c < kCPL; ++c) {
+      col[c] = c0 + c * 32 + lane;
+      cok[c] = col[c] < W;
+      acc[c] = cok[c] ? dst[r * W + col[c]] : T(0);
+    }
+    for (long long k0 = 0; k0 < L; k0 += 8) {
+      long long sr[8];
+      T v[kCPL][8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {   // eight rows in flight, then applied in order
+        const bool in = k0 + e < L;
+        long long sv = in ? (long long)perm[lo + k0 + e] : -1;
+        if (sv >= src_rows) sv = -1;   // cannot happen for a correct sort
+        sr[e] = sv;
+#pragma unroll
+        for (int c = 0; c < kCPL; ++c) v[c][e] = (sv >= 0 && cok[c]) ? __ldg(src + sv * W + col[c]) : T(0);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (sr[e] < 0) continue;
+#pragma unroll
+        for (int c = 0; c < kCPL; ++c) {
+          if (!cok[c]) continue;
+          if (prev) prev[sr[e] * W + col[c]] = acc[c];
+          acc[c] = acc[c] + v[c][e];
+        }
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < kCPL; ++c)
+      if (cok[c]) dst[r * W + col[c]] = acc[c];
+  }
+}
+
 // prev = +0.0 for source rows whose destination is outside [0, R).
 template <typename T>
 __global__ void rows_prev_skipped_kernel(const int32_t* __restrict__ idx, long long src_rows, long long offset,
@@ -99,7 +153,7 @@ extern "C" size_t det_scatter_add_rows_workspace_bytes(int64_t src_rows, int64_t
 
 template <typename T>
 static int rows_impl(T* dst, long long R, long long W, const int32_t* idx, long long off, const T* src, long long M,
-                     T* prev, void* ws, size_t ws_bytes, int bt, cudaStream_t s) {
+                     T* prev, void* ws, size_t ws_bytes, int bt, cudaStream_t s, bool ordered) {
   const SortPlan p = make_sort_plan(M, R, 0, true, bt);
   if (ws_bytes < p.total) return DET_ERR_WORKSPACE;
   if (M == 0 || W == 0) return cudaMemsetAsync(ws, 0, kHeaderBytes, s) == cudaSuccess ? DET_OK : DET_ERR_CUDA;
@@ -114,18 +168,22 @@ static int rows_impl(T* dst, long long R, long long W, const int32_t* idx, long 
     launch_end(s);
   }
   if (R > 0) {
-    launch_begin("det_rows", s);
-    rows_kernel<T><<<(unsigned)((R * 32 + 255) / 256), 256, 0, s>>>(
-        dst, R, W, src, reinterpret_cast<const int32_t*>(w + p.idx[fb]), reinterpret_cast<const int32_t*>(w + p.seg),
-        &h->n_valid, prev, M);
+    const int32_t* perm = reinterpret_cast<const int32_t*>(w + p.idx[fb]);
+    const int32_t* seg = reinterpret_cast<const int32_t*>(w + p.seg);
+    launch_begin(ordered ? "det_rows_ordered" : "det_rows", s);
+    if (ordered)
+      rows_ordered_kernel<T><<<(unsigned)((R * 32 + 255) / 256), 256, 0, s>>>(dst, R, W, src, perm, seg, &h->n_valid,
+                                                                               prev, M);
+    else
+      rows_kernel<T><<<(unsigned)((R * 32 + 255) / 256), 256, 0, s>>>(dst, R, W, src, perm, seg, &h->n_valid, prev, M);
     launch_end(s);
   }
   return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
 }
 
-extern "C" int det_scatter_add_rows(void* dst, int64_t dst_rows, int64_t row_len, const int32_t* idx,
-                                    int64_t row_offset, const void* src, int64_t src_rows, void* prev_out, int dtype,
-                                    void* workspace, size_t workspace_bytes, int block_threads, void* stream) {
+static int rows_entry(void* dst, int64_t dst_rows, int64_t row_len, const int32_t* idx, int64_t row_offset,
+                      const void* src, int64_t src_rows, void* prev_out, int dtype, void* workspace,
+                      size_t workspace_bytes, int block_threads, void* stream, bool ordered) {
   if (!valid_dtype(dtype)) return DET_ERR_DTYPE;
   if (dst_rows < 0 || row_len < 0 || src_rows < 0 || !workspace || !valid_block_threads(block_threads))
     return DET_ERR_INVALID_ARG;
@@ -135,7 +193,25 @@ extern "C" int det_scatter_add_rows(void* dst, int64_t dst_rows, int64_t row_len
   if (reinterpret_cast<uintptr_t>(workspace) % 256) return DET_ERR_WORKSPACE;
   if (dtype == DET_F32)
     return rows_impl<float>((float*)dst, dst_rows, row_len, idx, row_offset, (const float*)src, src_rows,
-                            (float*)prev_out, workspace, workspace_bytes, block_threads, as_stream(stream));
+                            (float*)prev_out, workspace, workspace_bytes, block_threads, as_stream(stream), ordered);
   return rows_impl<double>((double*)dst, dst_rows, row_len, idx, row_offset, (const double*)src, src_rows,
-                           (double*)prev_out, workspace, workspace_bytes, block_threads, as_stream(stream));
+                           (double*)prev_out, workspace, workspace_bytes, block_threads, as_stream(stream), ordered);
+}
+
+extern "C" int det_scatter_add_rows(void* dst, int64_t dst_rows, int64_t row_len, const int32_t* idx,
+                                    int64_t row_offset, const void* src, int64_t src_rows, void* prev_out, int dtype,
+                                    void* workspace, size_t workspace_bytes, int block_threads, void* stream) {
+  return rows_entry(dst, dst_rows, row_len, idx, row_offset, src, src_rows, prev_out, dtype, workspace,
+                    workspace_bytes, block_threads, stream, false);
+}
+
+// The ordered reading of "returns the previous value": source rows applied
+// one at a time in ascending order (Warp language reference
+// "warp.tile_atomic_add_indexed", returns).
+extern "C" int det_scatter_add_rows_ordered(void* dst, int64_t dst_rows, int64_t row_len, const int32_t* idx,
+                                            int64_t row_offset, const void* src, int64_t src_rows, void* prev_out,
+                                            int dtype, void* workspace, size_t workspace_bytes, int block_threads,
+                                            void* stream) {
+  return rows_entry(dst, dst_rows, row_len, idx, row_offset, src, src_rows, prev_out, dtype, workspace,
+                    workspace_bytes, block_threads, stream, true);
 }

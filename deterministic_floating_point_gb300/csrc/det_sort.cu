@@ -616,7 +616,7 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
                     long long* __restrict__ blocks, LongSeg* __restrict__ lsegs, unsigned int* __restrict__ ldone,
                     unsigned int* __restrict__ nblocks, unsigned int* __restrict__ nlsegs,
                     const unsigned int* __restrict__ n_valid, long long max_blocks, long long max_lsegs,
-                    unsigned int* __restrict__ status) {
+                    unsigned int* __restrict__ status, long long ostride) {
   const long long b = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (b >= m) return;
@@ -626,7 +626,7 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
   if (len <= 0) return;
   if (len <= kSegBlock) {
     const T t = warp_pt_range<T, false, NEG>(vals + lo, len);
-    if (lane == 0) out[b] = out[b] + t;
+    if (lane == 0) out[b * ostride] = out[b * ostride] + t;
     return;
   }
   const long long nblk = (len + kSegBlock - 1) / kSegBlock;
@@ -660,7 +660,8 @@ __global__ void __launch_bounds__(256)
 segtree_blocks_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg, const long long* __restrict__ blocks,
                       const unsigned int* __restrict__ nblocks, const LongSeg* __restrict__ lsegs,
                       unsigned int* __restrict__ ldone, T* nodes, T* __restrict__ out,
-                      const unsigned int* __restrict__ n_valid, long long max_blocks, long long max_lsegs) {
+                      const unsigned int* __restrict__ n_valid, long long max_blocks, long long max_lsegs,
+                      long long ostride) {
   static_assert(kSegBlock == 256 * 8, "one CTA of 256 threads x 8 leaves per block");
   __shared__ __align__(16) T buf[kSegBlock];
   __shared__ T wnode[8];
@@ -702,7 +703,7 @@ segtree_blocks_kernel(const T* __restrict__ vals, const int32_t* __restrict__ se
   if (last && tid < 32) {
     __threadfence();
     const T t = warp_pt_range<T, true>(nodes + L.base, L.nblk);   // nodes already hold the negated leaves
-    if (tid == 0) out[L.bin] = out[L.bin] + t;
+    if (tid == 0) out[L.bin * ostride] = out[L.bin * ostride] + t;
   }
 }
 
@@ -859,7 +860,8 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
 }
 
 template <typename T>
-int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T* out, cudaStream_t s, bool negate) {
+int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T* out, cudaStream_t s, bool negate,
+                           long long ostride, bool reset_counters) {
   if (p.n == 0 || p.m == 0) return DET_OK;
   char* w = reinterpret_cast<char*>(ws);
   SortHdr* h = reinterpret_cast<SortHdr*>(ws);
@@ -868,21 +870,25 @@ int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T*
   LongSeg* lsegs = reinterpret_cast<LongSeg*>(w + p.lsegs);
   T* nodes = reinterpret_cast<T*>(w + p.nodes);
   unsigned int* ldone = reinterpret_cast<unsigned int*>(w + p.ldone);
+  if (reset_counters && cudaMemsetAsync(&h->long_blocks, 0, 2 * sizeof(unsigned int), s) != cudaSuccess)
+    return DET_ERR_CUDA;
   launch_begin("det_segtree_bins", s);
   auto* kb = negate ? segtree_bins_kernel<T, true> : segtree_bins_kernel<T, false>;
   kb<<<(unsigned)((p.m * 32 + 255) / 256), 256, 0, s>>>(sorted_vals, seg, p.m, out, blocks, lsegs, ldone,
                                                          &h->long_blocks, &h->long_segs, &h->n_valid, p.max_blocks,
-                                                         p.max_lsegs, &h->status);
+                                                         p.max_lsegs, &h->status, ostride);
   launch_end(s);
   launch_begin("det_segtree_blocks", s);
   auto* kk = negate ? segtree_blocks_kernel<T, true> : segtree_blocks_kernel<T, false>;
   kk<<<(unsigned)p.max_blocks, 256, 0, s>>>(sorted_vals, seg, blocks, &h->long_blocks, lsegs, ldone, nodes, out,
-                                            &h->n_valid, p.max_blocks, p.max_lsegs);
+                                            &h->n_valid, p.max_blocks, p.max_lsegs, ostride);
   launch_end(s);
   return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
 }
 
-template int enqueue_segmented_tree<float>(const SortPlan&, void*, const float*, float*, cudaStream_t, bool);
-template int enqueue_segmented_tree<double>(const SortPlan&, void*, const double*, double*, cudaStream_t, bool);
+template int enqueue_segmented_tree<float>(const SortPlan&, void*, const float*, float*, cudaStream_t, bool, long long,
+                                           bool);
+template int enqueue_segmented_tree<double>(const SortPlan&, void*, const double*, double*, cudaStream_t, bool,
+                                            long long, bool);
 
 }  // namespace det

@@ -56,7 +56,9 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
 // Segmented pairwise tree: out[b] = out[b] + PT(vals[seg[b] .. seg[b+1]))
 // for every non-empty b.  T is float or double.
 template <typename T>
+// out[b * ostride] receives bin b; reset_counters clears the long-bin
+// counters of the header (needed when the same sort feeds several trees).
 int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T* out, cudaStream_t s,
-                           bool negate = false);
+                           bool negate = false, long long ostride = 1, bool reset_counters = false);
 
 }  // namespace det

@@ -40,6 +40,9 @@ _SIGNATURES = {
     "det_scan": (_int, [_vp, _vp, _i64, _int, _int, _vp, _vp, _sz, _int, _vp]),
     "det_segmented_scan_workspace_bytes": (_sz, [_i64, _i64, _int]),
     "det_segmented_scan": (_int, [_vp, _vp, _i64, _vp, _i64, _int, _int, _vp, _sz, _int, _vp]),
+    "det_scatter_add_rows_ordered": (_int, [_vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _int, _vp, _sz, _int, _vp]),
+    "det_scatter_add_vec_workspace_bytes": (_sz, [_i64, _i64, _i64, _int]),
+    "det_scatter_add_vec": (_int, [_vp, _i64, _i64, _vp, _vp, _i64, _int, _vp, _sz, _int, _vp]),
     "det_scatter_sub": (_int, [_vp, _i64, _vp, _vp, _i64, _int, _vp, _vp, _vp, _sz, _int, _vp]),
     "det_scatter_minmax_workspace_bytes": (_sz, [_i64, _int]),
     "det_scatter_min": (_int, [_vp, _i64, _vp, _vp, _i64, _int, _vp, _sz, _int, _vp]),
@@ -277,8 +280,13 @@ def det_slot_alloc(counter: torch.Tensor, index: torch.Tensor, *, count: torch.T
 
 def det_scatter_add_rows(dst: torch.Tensor, idx: torch.Tensor, src: torch.Tensor, *, row_offset: int = 0,
                          prev_out: torch.Tensor | None = None, block_threads: int = 0,
-                         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """dst[idx[s] + row_offset] += src[s] row by row, in a fixed order; returns dst."""
+                         workspace: torch.Tensor | None = None, stream=None, ordered: bool = False) -> torch.Tensor:
+    """dst[idx[s] + row_offset] += src[s] row by row, in a fixed order; returns dst.
+
+    ordered=False: per destination the rows are added by the pairwise tree and
+    every contributor's prev is the row before the call.  ordered=True: the
+    rows are applied one at a time in ascending s and prev is the running value
+    (det_scatter_add_rows_ordered)."""
     _dev(dst, "dst"), _dev(idx, "idx"), _dev(src, "src")
     code = _code(src)
     if dst.dim() != 2 or src.dim() != 2 or dst.shape[1] != src.shape[1] or dst.dtype != src.dtype:
@@ -289,10 +297,27 @@ def det_scatter_add_rows(dst: torch.Tensor, idx: torch.Tensor, src: torch.Tensor
     M = src.shape[0]
     nbytes = lib().det_scatter_add_rows_workspace_bytes(M, R, W, code)
     ws = _ws(workspace, nbytes, src.device)
-    _check(lib().det_scatter_add_rows(_ptr(dst), R, W, _ptr(idx), int(row_offset), _ptr(src), M,
-                                      _ptr(prev_out), code, _ptr(ws), ws.numel(), block_threads,
-                                      _stream(stream)), "det_scatter_add_rows")
+    fn = "det_scatter_add_rows_ordered" if ordered else "det_scatter_add_rows"
+    _check(getattr(lib(), fn)(_ptr(dst), R, W, _ptr(idx), int(row_offset), _ptr(src), M, _ptr(prev_out), code,
+                              _ptr(ws), ws.numel(), block_threads, _stream(stream)), fn)
     return dst
+
+
+def det_scatter_add_vec(out: torch.Tensor, bins: torch.Tensor, values: torch.Tensor, *, block_threads: int = 0,
+                        workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[bins[i], :] += values[i, :] for composite values, component-wise in a fixed order; returns out."""
+    _dev(out, "out"), _dev(bins, "bins"), _dev(values, "values")
+    code = _code(values)
+    if out.dim() != 2 or values.dim() != 2 or out.shape[1] != values.shape[1] or out.dtype != values.dtype:
+        raise ValueError("out and values must be 2-D of one dtype with equal width")
+    if bins.dtype != torch.int32 or bins.numel() != values.shape[0]:
+        raise ValueError("bins must be int32 with one entry per record")
+    m, width = out.shape
+    n = values.shape[0]
+    ws = _ws(workspace, lib().det_scatter_add_vec_workspace_bytes(n, m, width, code), values.device)
+    _check(lib().det_scatter_add_vec(_ptr(out), m, width, _ptr(bins), _ptr(values), n, code, _ptr(ws), ws.numel(),
+                                     block_threads, _stream(stream)), "det_scatter_add_vec")
+    return out
 
 
 def det_scan(x: torch.Tensor, y: torch.Tensor | None = None, *, flags: int = SCAN_INCLUSIVE,

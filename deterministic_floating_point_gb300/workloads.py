@@ -124,3 +124,17 @@ def rows_input(src_rows: int = ROWS_SRC, dst_rows: int = ROWS_DST, row_len: int 
     idx = rng.integers(0, dst_rows, src_rows, dtype=np.int32)
     dst = _cast(rng.standard_normal((dst_rows, row_len)), dtype)
     return src, idx, dst
+
+
+VEC_WIDTH = 3
+
+
+def vec_scatter_input(n: int = SCATTER_N, width: int = VEC_WIDTH, num_bins: int = SCATTER_BINS, dtype=np.float32,
+                      seed: int = 6):
+    """Composite scatter records (vec3 by default): returns (values n x width, bins, out0 num_bins x width),
+    values N(0,1), bins uniform, out0 zero-initialised like the scalar scatter's."""
+    rng = np.random.default_rng(seed)
+    values = _cast(rng.standard_normal((n, width)), dtype)
+    bins = rng.integers(0, num_bins, n, dtype=np.int32)
+    out0 = np.zeros((num_bins, width), dtype=dtype)
+    return values, bins, out0

@@ -209,6 +209,44 @@ int det_scatter_add_rows(void* dst, int64_t dst_rows, int64_t row_len, const int
                          void* stream);
 
 /* ------------------------------------------------------------------------
+ * det_scatter_add_rows_ordered -- det_scatter_add_rows with the other
+ * reading of "returns the previous value": the source rows aimed at one
+ * destination are applied one at a time in ascending s (atomics in thread
+ * order).  prev_out[s] receives the destination row just before row s is
+ * added (the running prefix in index order), and the destination ends at the
+ * sequential sum old + v_0 + v_1 + ... (left to right).  Arguments, layout,
+ * workspace (det_scatter_add_rows_workspace_bytes), limits and errors as
+ * det_scatter_add_rows.
+ * Follows: Warp language reference "warp.tile_atomic_add_indexed" (returns:
+ * the previous values, unspecified under repeats).
+ */
+int det_scatter_add_rows_ordered(void* dst, int64_t dst_rows, int64_t row_len, const int32_t* idx,
+                                 int64_t row_offset, const void* src, int64_t src_rows, void* prev_out,
+                                 int dtype, void* workspace, size_t workspace_bytes, int block_threads,
+                                 void* stream);
+
+/* ------------------------------------------------------------------------
+ * det_scatter_add_vec -- composite values (vec3, mat33, quaternions, ...:
+ * `width` components per record) scattered with wp.atomic_add's
+ * deterministic form: for every bin b with records and every component c,
+ * out[b][c] = out[b][c] + PT(component c of group b), the groups in
+ * ascending record index (exactly det_scatter_add per component, and
+ * det_scatter_add_rows with row_len = width and no prev).
+ *   out     device, out_len x width elements of dtype, row-major (read and written)
+ *   bins    device, n int32 (outside [0, out_len): skipped)
+ *   values  device, n x width elements of dtype, row-major
+ * Workspace: det_scatter_add_vec_workspace_bytes(n, out_len, width, dtype).
+ * Limits: n <= DET_MAX_RECORDS, out_len <= 2^31 - 1, width <= 4096.
+ * Follows: Warp user guide "Deterministic Execution", "Pattern 1:
+ * Accumulation" (vectors, matrices, quaternions and transforms take the
+ * segmented reduction path) and "Picking the Right Mode" (composite values).
+ */
+size_t det_scatter_add_vec_workspace_bytes(int64_t n, int64_t out_len, int64_t width, int dtype);
+int det_scatter_add_vec(void* out, int64_t out_len, int64_t width, const int32_t* bins, const void* values,
+                        int64_t n, int dtype, void* workspace, size_t workspace_bytes, int block_threads,
+                        void* stream);
+
+/* ------------------------------------------------------------------------
  * det_scan -- prefix sum by a single-pass decoupled look-back whose
  * look-back is anchored: chunks of DET_SCAN_CHUNK_* elements, intervals of
  * 32 chunks; look-back lane l of chunk c = 32k + j reads the aggregate of

@@ -204,3 +204,50 @@ def test_slot_alloc_at_bench_size(det):
     ctr = torch.zeros(1, dtype=torch.int32, device="cuda")
     slots = det.det_slot_alloc(ctr, _cuda(idx))
     assert np.array_equal(slots.cpu().numpy(), want_slots) and int(ctr.item()) == int(want_ctr[0])
+
+
+# ---------------------------------------------------------------------------
+# composite values and the ordered row scatter
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("width", [1, 3, 4, 9])
+def test_scatter_add_vec(det, dtype, width):
+    rng = np.random.default_rng(40 + width)
+    n, m = 300_007, 777
+    values = rng.standard_normal((n, width)).astype(dtype)
+    bins = rng.integers(-5, m + 5, n).astype(np.int32)
+    bins[:100_000] = 3                                     # one long group: block trees + merge
+    out0 = rng.standard_normal((m, width)).astype(dtype)
+    want, _ = oracle.det_scatter_add_rows(out0, bins, values)
+    for bt in (128, 256, 1024):
+        out = _cuda(out0.copy())
+        det.det_scatter_add_vec(out, _cuda(bins), _cuda(values), block_threads=bt)
+        assert np.array_equal(_bits(out.cpu().numpy()), _bits(want))
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("W", [1, 3, 64, 100])
+def test_scatter_add_rows_ordered(det, dtype, W):
+    rng = np.random.default_rng(50 + W)
+    M, R = 40_003, 1_500
+    src = rng.standard_normal((M, W)).astype(dtype)
+    idx = rng.integers(-3, R + 3, M).astype(np.int32)
+    idx[:3000] = 7                                         # a long run on one destination
+    dst0 = rng.standard_normal((R, W)).astype(dtype)
+    want, want_prev = oracle.det_scatter_add_rows_ordered(dst0, idx, src)
+    for bt in (128, 256):
+        dst = _cuda(dst0.copy())
+        prev = torch.empty(src.shape, dtype=dst.dtype, device="cuda")
+        det.det_scatter_add_rows(dst, _cuda(idx), _cuda(src), prev_out=prev, ordered=True, block_threads=bt)
+        assert np.array_equal(_bits(dst.cpu().numpy()), _bits(want))
+        assert np.array_equal(_bits(prev.cpu().numpy()), _bits(want_prev))
+
+
+def test_rows_ordered_at_bench_size(det):
+    src, idx, dst0 = workloads.rows_input(dtype=np.float32)
+    want, want_prev = oracle.det_scatter_add_rows_ordered(dst0, idx, src)
+    dst = _cuda(dst0.copy())
+    prev = torch.empty(src.shape, dtype=dst.dtype, device="cuda")
+    det.det_scatter_add_rows(dst, _cuda(idx), _cuda(src), prev_out=prev, ordered=True)
+    assert np.array_equal(_bits(dst.cpu().numpy()), _bits(want))
+    assert np.array_equal(_bits(prev.cpu().numpy()), _bits(want_prev))
