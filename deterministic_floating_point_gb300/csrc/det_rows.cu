@@ -32,46 +32,63 @@ rows_kernel(T* __restrict__ dst, long long R, long long W, const T* __restrict__
   const long long hi = min((long long)seg[r + 1], N), lo = max(0LL, min((long long)seg[r], hi));
   const long long L = hi - lo;
   if (L <= 0) return;
+  const bool small = L <= 32;   // at most four rounds: their level-3 nodes are combined by a fixed tree
   for (long long c0 = 0; c0 < W; c0 += 32 * kCPL) {
     long long col[kCPL];
     bool cok[kCPL];
+    T old[kCPL];
 #pragma unroll
     for (int c = 0; c < kCPL; ++c) {
       col[c] = c0 + c * 32 + lane;
       cok[c] = col[c] < W;
+      old[c] = cok[c] ? dst[r * W + col[c]] : T(0);   // the row before the call: every contributor's prev
     }
-    NodeCounter<T, 8> nc[kCPL];
+    T n4[kCPL][4];
+#pragma unroll
+    for (int c = 0; c < kCPL; ++c)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) n4[c][q] = absent<T>();
+    NodeCounter<T, 1> nc[kCPL];   // groups of more than 32 rows only (rare): deeper levels in local memory
     for (long long k0 = 0; k0 < L; k0 += 8) {
+      int sr[8];
       T v[kCPL][8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const bool in = k0 + e < L;
-        long long s = in ? (long long)perm[lo + k0 + e] : 0;
-        if (s < 0 || s >= src_rows) s = 0;   // cannot happen for a correct sort
-#pragma unroll
-        for (int c = 0; c < kCPL; ++c) v[c][e] = (in && cok[c]) ? __ldg(src + s * W + col[c]) : absent<T>();
-      }
-#pragma unroll
-      for (int c = 0; c < kCPL; ++c) nc[c].push(thread_pt(v[c]));   // 8 rows -> level-3 node
-    }
-    T tree[kCPL];
-#pragma unroll
-    for (int c = 0; c < kCPL; ++c) tree[c] = nc[c].result();
-    T old[kCPL];
-#pragma unroll
-    for (int c = 0; c < kCPL; ++c) old[c] = cok[c] ? dst[r * W + col[c]] : T(0);
-    if (prev) {
-      for (long long k = 0; k < L; ++k) {
-        long long s = perm[lo + k];
-        if (s < 0 || s >= src_rows) continue;
+        int sv = in ? perm[lo + k0 + e] : -1;
+        if ((long long)sv >= src_rows) sv = -1;   // cannot happen for a correct sort
+        sr[e] = sv;
 #pragma unroll
         for (int c = 0; c < kCPL; ++c)
-          if (cok[c]) prev[s * W + col[c]] = old[c];
+          v[c][e] = (sv >= 0 && cok[c]) ? __ldg(src + (long long)sv * W + col[c]) : absent<T>();
+      }
+      if (prev) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (sr[e] < 0) continue;
+#pragma unroll
+          for (int c = 0; c < kCPL; ++c)
+            if (cok[c]) prev[(long long)sr[e] * W + col[c]] = old[c];
+        }
+      }
+      const int q = (int)(k0 >> 3);
+#pragma unroll
+      for (int c = 0; c < kCPL; ++c) {
+        const T node = thread_pt(v[c]);   // 8 rows -> level-3 node
+        if (small) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (j == q) n4[c][j] = node;
+        } else {
+          nc[c].push(node);
+        }
       }
     }
 #pragma unroll
-    for (int c = 0; c < kCPL; ++c)
-      if (cok[c]) dst[r * W + col[c]] = old[c] + tree[c];
+    for (int c = 0; c < kCPL; ++c) {
+      const T tree = small ? (n4[c][0] + n4[c][1]) + (n4[c][2] + n4[c][3]) : nc[c].result();
+      if (cok[c]) dst[r * W + col[c]] = old[c] + tree;
+    }
   }
 }
 
