@@ -58,6 +58,7 @@ def _load():
                 getattr(lib, f"oracle_scan_{sfx}").argtypes = [vp, vp, i64, ctypes.c_int, vp]
                 getattr(lib, f"oracle_segmented_scan_{sfx}").argtypes = [vp, vp, i64, vp, i64, ctypes.c_int]
                 getattr(lib, f"oracle_scatter_sub_{sfx}").argtypes = [vp, i64, vp, vp, i64]
+                getattr(lib, f"oracle_gather_rows_{sfx}").argtypes = [vp, vp, i64, i64, vp, i64, i64]
                 getattr(lib, f"oracle_scatter_add_rows_ordered_{sfx}").argtypes = [vp, i64, i64, vp, i64, vp, i64, vp]
                 getattr(lib, f"oracle_scatter_minmax_{sfx}").argtypes = [vp, i64, vp, vp, i64, ctypes.c_int]
             lib.oracle_scan_i32.argtypes = [vp, vp, i64, ctypes.c_int, vp]
@@ -234,3 +235,16 @@ def det_scatter_add_rows_ordered(dst: np.ndarray, idx: np.ndarray, src: np.ndarr
         _ptr(res), res.shape[0], res.shape[1], _ptr(idx), int(row_offset), _ptr(src), src.shape[0], _ptr(prev))
     _check(rc, "scatter_add_rows_ordered")
     return res, prev
+
+
+def det_gather_rows(src: np.ndarray, idx: np.ndarray, row_offset: int = 0):
+    """out[i] = src[idx[i] + row_offset] (+0.0 rows for indices outside src); src is 1-D or 2-D."""
+    src = np.ascontiguousarray(src)
+    sfx = _sfx(src.dtype)
+    src2 = src.reshape(src.shape[0], -1) if src.ndim != 1 else src.reshape(-1, 1)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    out = np.empty((idx.size, src2.shape[1]), dtype=src.dtype)
+    rc = getattr(_load(), f"oracle_gather_rows_{sfx}")(_ptr(out), _ptr(src2), src2.shape[0], src2.shape[1],
+                                                        _ptr(idx), int(row_offset), idx.size)
+    _check(rc, "gather_rows")
+    return out.reshape(-1) if src.ndim == 1 else out

@@ -247,6 +247,23 @@ int FN(oracle_scatter_add_rows_ordered)(T* dst, int64_t dst_rows, int64_t row_le
     return 0;
 }
 
+/* det_gather_rows: out[i] = src[idx[i] + row_offset] row by row, +0.0 for
+ * indices outside [0, src_rows) -- the forward gather of Warp "Deterministic
+ * Execution", "Tape and Backward Passes" (out[tid] = values[indices[tid]]),
+ * whose adjoint is det_scatter_add_rows of the output gradient. */
+int FN(oracle_gather_rows)(T* out, const T* src, int64_t src_rows, int64_t row_len, const int32_t* idx,
+                           int64_t row_offset, int64_t n)
+{
+    if (src_rows < 0 || row_len < 0 || n < 0) return 1;
+    if (n > 0 && row_len > 0 && (!out || !idx || (src_rows > 0 && !src))) return 1;
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t r = (int64_t)idx[i] + row_offset;
+        for (int64_t j = 0; j < row_len; ++j)
+            out[i * row_len + j] = (r >= 0 && r < src_rows) ? src[r * row_len + j] : (T)0.0;
+    }
+    return 0;
+}
+
 /* ---------------------------------------------------------------------- */
 /* Anchored decoupled look-back scan (drjit-core pull request "Make CUDA
  * floating-point prefix sums deterministic", sections "Implementation" and

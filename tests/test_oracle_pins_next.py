@@ -1,5 +1,5 @@
 """CPU pins of the oracle's scatter-sub, scatter-min/max, int32 scan, slot
-allocation and the ordered row scatter against facts the pages and the mathematics fix, computed here
+allocation, the ordered row scatter and the gather against facts the pages and the mathematics fix, computed here
 without the oracle: integer-exact sums, numpy's grouped minimum/maximum, numpy
 cumulative sums with int32 wrap-around, the pages' compaction example
 (Warp "Deterministic Execution", "Pattern 2: Slot Allocation" and "Picking the
@@ -240,3 +240,21 @@ def test_rows_ordered_equals_default_for_distinct_rows():
     b = oracle.det_scatter_add_rows(dst0, idx, src)
     assert np.array_equal(_bits(a[0]), _bits(b[0])) and np.array_equal(_bits(a[1]), _bits(b[1]))
     assert np.array_equal(a[1], dst0[idx])
+
+
+# ---------------------------------------------------------------------------
+# gather (the forward of the pages' backward example)
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+def test_gather_matches_numpy_take(dtype):
+    rng = np.random.default_rng(34)
+    src = rng.standard_normal((300, 7)).astype(dtype)
+    idx = rng.integers(-5, 305, 2000).astype(np.int32)
+    got = oracle.det_gather_rows(src, idx)
+    ok = (idx >= 0) & (idx < 300)
+    want = np.zeros((2000, 7), dtype)
+    want[ok] = src[idx[ok]]
+    assert np.array_equal(_bits(got), _bits(want))
+    v = src[:, 0].copy()
+    assert np.array_equal(_bits(oracle.det_gather_rows(v, idx)), _bits(want[:, 0]))
+    assert np.array_equal(oracle.det_gather_rows(src, idx + 3, row_offset=-3), got)
