@@ -259,6 +259,49 @@ def build_workload(name, torch, det, dev):
                     config={"workload": f"det_scatter_add_vec n={n} vec{W} N(0,1) {dt}, {m} uniform bins, seed 6",
                             "n": n, "width": W, "bins": m, "l2": "L2 flushed between timed steps"})
 
+    if name == "gather_grad":
+        # the pages' backward example at the row workload's sizes: out = table[idx] forward,
+        # table.grad[idx] += grad_out backward (det_gather_rows, then det_scatter_add_rows)
+        from deterministic_floating_point_gb300 import autograd
+        gout_np, idx_np, table_np = workloads.rows_input(dtype=npdt)
+        M, W = gout_np.shape
+        R = table_np.shape[0]
+        table = torch.from_numpy(table_np).to(dev).requires_grad_(True)
+        idx = torch.from_numpy(idx_np).to(dev)
+        gout = torch.from_numpy(gout_np).to(dev)
+        s = gout_np.itemsize
+        host_g = torch.from_numpy(gout_np).pin_memory()
+        host_grad = torch.empty_like(table, device="cpu").pin_memory()
+
+        def step():
+            table.grad = None
+            autograd.gather(table, idx).backward(gout)
+
+        def e2e_step():
+            gout.copy_(host_g, non_blocking=True)
+            step()
+            host_grad.copy_(table.grad, non_blocking=True)
+
+        def oracle_sample():
+            import oracle
+            k = 1 << 17
+            z = np.zeros_like(table_np)
+
+            def f():
+                oracle.det_gather_rows(table_np, idx_np[:k])
+                oracle.det_scatter_add_rows(z, idx_np[:k], gout_np[:k])
+            reps, secs = _timed_oracle(f)
+            return k * W * reps, secs, f"{reps} x gather + adjoint scatter of the first {k} rows, 1 thread"
+
+        # forward: read table rows, write out; backward: read grad_out, table.grad in/out, sorted ids
+        bwd_bytes = M * W * s + 2 * R * W * s + 4 * M
+        return dict(state={"table": table, "idx": idx, "gout": gout}, step=step, elems=M * W, algo_bytes=bwd_bytes,
+                    step_bytes=2 * M * W * s + bwd_bytes, dominant="det_rows", dtype=dt, e2e_step=e2e_step,
+                    h2d=M * W * s, d2h=R * W * s, oracle_sample=oracle_sample,
+                    config={"workload": f"autograd gather of {M} rows x {W} {dt} from a {R}-row table + backward "
+                                        "(rows workload inputs, seed 5)", "rows": M, "table_rows": R, "row_len": W,
+                            "l2": "L2 flushed between timed steps"})
+
     if name == "scan_i32":
         n = N_OVERRIDE or workloads.SCAN_N
         # count -> exclusive scan -> write: 0/1 flags of the scan workload's values
@@ -518,6 +561,9 @@ def add_checks(name, wl, torch, det, dev):
             wl["base_once"] = b1
             wl["base_step"] = lambda: det.atomic_scatter_add(out, b, nv)
             wl["base_name"] = "atomic_scatter_add of -values"
+    elif name == "gather_grad":
+        table = st["table"]
+        wl["det_once"] = lambda: (wl["step"](), fingerprint(torch, table.grad))[1]
     elif name == "scan_i32":
         y = st["y"]
         wl["det_once"] = lambda: (wl["step"](), fingerprint(torch, y))[1]
@@ -633,7 +679,7 @@ def traffic_for(kernel, workload):
 
 OPS = ["sum", "sum_f64", "sum_small", "scatter_f64", "scatter_bin0", "skew", "skew_f32", "scan", "scan_f64",
        "scan_small", "segscan", "rows", "scatter_sub", "scatter_min", "scatter_max", "scan_i32", "slot_alloc",
-       "slot_alloc_multi", "scatter_vec3", "rows_ordered"]
+       "slot_alloc_multi", "scatter_vec3", "rows_ordered", "gather_grad"]
 
 
 def measure_op(name, torch, det, dev, flush, steps, runs, peak):

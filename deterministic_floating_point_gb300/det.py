@@ -43,6 +43,7 @@ _SIGNATURES = {
     "det_scatter_add_rows_ordered": (_int, [_vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _int, _vp, _sz, _int, _vp]),
     "det_scatter_add_vec_workspace_bytes": (_sz, [_i64, _i64, _i64, _int]),
     "det_scatter_add_vec": (_int, [_vp, _i64, _i64, _vp, _vp, _i64, _int, _vp, _sz, _int, _vp]),
+    "det_gather_rows": (_int, [_vp, _vp, _i64, _i64, _vp, _i64, _i64, _int, _int, _vp]),
     "det_scatter_sub": (_int, [_vp, _i64, _vp, _vp, _i64, _int, _vp, _vp, _vp, _sz, _int, _vp]),
     "det_scatter_minmax_workspace_bytes": (_sz, [_i64, _int]),
     "det_scatter_min": (_int, [_vp, _i64, _vp, _vp, _i64, _int, _vp, _sz, _int, _vp]),
@@ -192,6 +193,22 @@ def det_scatter_add(out: torch.Tensor, bins: torch.Tensor, values: torch.Tensor,
     _check(lib().det_scatter_add(_ptr(out), m, _ptr(bins), _ptr(values), n, code, _ptr(perm_out),
                                  _ptr(seg_offsets_out), _ptr(ws), ws.numel(), block_threads,
                                  _stream(stream)), "det_scatter_add")
+    return out
+
+
+def det_gather_rows(src: torch.Tensor, idx: torch.Tensor, out: torch.Tensor | None = None, *, row_offset: int = 0,
+                    block_threads: int = 0, stream=None) -> torch.Tensor:
+    """out[i] = src[idx[i] + row_offset] (zeros outside src); src is 1-D (scalars) or 2-D (rows)."""
+    _dev(src, "src"), _dev(idx, "idx")
+    code = _code(src)
+    if idx.dtype != torch.int32:
+        raise TypeError("idx must be int32")
+    W = 1 if src.dim() == 1 else src.shape[1]
+    n = idx.numel()
+    if out is None:
+        out = torch.empty((n,) if src.dim() == 1 else (n, W), dtype=src.dtype, device=src.device)
+    _check(lib().det_gather_rows(_ptr(out), _ptr(src), src.shape[0], W, _ptr(idx), int(row_offset), n, code,
+                                 block_threads, _stream(stream)), "det_gather_rows")
     return out
 
 

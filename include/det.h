@@ -247,6 +247,23 @@ int det_scatter_add_vec(void* out, int64_t out_len, int64_t width, const int32_t
                         void* stream);
 
 /* ------------------------------------------------------------------------
+ * det_gather_rows -- out[i] = src[idx[i] + row_offset] row by row, +0.0 rows
+ * for indices outside [0, src_rows).  Nothing is combined, so the result is
+ * schedule-free.  It is the forward of the pages' backward example: its
+ * adjoint, grad_src[idx[i]] += grad_out[i], is det_scatter_add_rows
+ * (det_scatter_add for row_len 1), which makes the reverse pass
+ * deterministic too.
+ *   out  device, n x row_len elements of dtype (written)
+ *   src  device, src_rows x row_len elements of dtype
+ *   idx  device, n int32
+ * No workspace.  block_threads 128 gives 128-thread CTAs, any other value 256.
+ * Follows: Warp user guide "Deterministic Execution", "Tape and Backward
+ * Passes" (gather: out[tid] = values[indices[tid]]).
+ */
+int det_gather_rows(void* out, const void* src, int64_t src_rows, int64_t row_len, const int32_t* idx,
+                    int64_t row_offset, int64_t n, int dtype, int block_threads, void* stream);
+
+/* ------------------------------------------------------------------------
  * det_scan -- prefix sum by a single-pass decoupled look-back whose
  * look-back is anchored: chunks of DET_SCAN_CHUNK_* elements, intervals of
  * 32 chunks; look-back lane l of chunk c = 32k + j reads the aggregate of
