@@ -8,10 +8,11 @@
 // repeats.  Here:
 //   1. the row indices are sorted stably (payload: the source row id), so
 //      the rows aimed at one destination are in ascending source order;
-//   2. one warp per destination row reduces those rows column by column with
-//      the pairwise tree over their rank (rounds of 8 rows in registers,
-//      a binary counter across rounds), reads the old row once, writes it to
-//      prev for every contributor, and stores old + tree;
+//   2. one warp per destination row reads the old row, then reduces the rows
+//      column by column with the pairwise tree over their rank (rounds of 8
+//      rows in registers; up to four rounds combined by a fixed tree, a
+//      binary counter beyond), writes the old row to prev for every
+//      contributor as it goes, and stores old + tree;
 //   3. skipped source rows get prev = +0.0.
 #include "det_sort.cuh"
 
