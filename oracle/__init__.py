@@ -30,6 +30,7 @@ _lib = None
 SCAN_INCLUSIVE = 0
 SCAN_EXCLUSIVE = 1
 SCAN_REVERSE = 2
+SCAN_SEGMENT_RESTART = 4
 
 
 def build(force: bool = False) -> str:

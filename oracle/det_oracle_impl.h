@@ -500,12 +500,23 @@ static void FN(segscan_incl_forward)(const T* x, const unsigned char* head, T* y
 int FN(oracle_segmented_scan)(const T* x, T* y, int64_t n, const int64_t* offsets,
                               int64_t num_segments, int flags)
 {
-    if (n < 0 || num_segments < 0 || (flags & ~3)) return 1;
+    if (n < 0 || num_segments < 0 || (flags & ~7)) return 1;
     if (n > 0 && (!x || !y || !offsets || num_segments < 1)) return 1;
     if (offsets) {
         if (offsets[0] != 0 || offsets[num_segments] != n) return 1;
         for (int64_t s = 0; s < num_segments; ++s)
             if (offsets[s + 1] < offsets[s]) return 1;
+    }
+    if (flags & 4) {
+        /* Per-segment restart (flag 4): every segment is det_scan of the
+         * segment alone -- its own chunk grid, look-back and anchors from the
+         * segment's first element (the other reading of "segmented scans" in
+         * the drjit-core pull request, "Validation"). */
+        for (int64_t s = 0; s < num_segments; ++s) {
+            const int64_t a = offsets[s], len = offsets[s + 1] - offsets[s];
+            if (len > 0) FN(oracle_scan)(x + a, y + a, len, flags & 3, NULL);
+        }
+        return 0;
     }
     int exclusive = flags & 1, reverse = flags & 2;
     unsigned char* head = (unsigned char*)calloc((size_t)n + 1, 1);

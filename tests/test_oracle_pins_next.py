@@ -1,5 +1,6 @@
 """CPU pins of the oracle's scatter-sub, scatter-min/max, int32 scan, slot
-allocation, the ordered row scatter and the gather against facts the pages and the mathematics fix, computed here
+allocation, the ordered row scatter, the gather and the per-segment-restart
+segmented scan against facts the pages and the mathematics fix, computed here
 without the oracle: integer-exact sums, numpy's grouped minimum/maximum, numpy
 cumulative sums with int32 wrap-around, the pages' compaction example
 (Warp "Deterministic Execution", "Pattern 2: Slot Allocation" and "Picking the
@@ -258,3 +259,66 @@ def test_gather_matches_numpy_take(dtype):
     v = src[:, 0].copy()
     assert np.array_equal(_bits(oracle.det_gather_rows(v, idx)), _bits(want[:, 0]))
     assert np.array_equal(oracle.det_gather_rows(src, idx + 3, row_offset=-3), got)
+
+
+# ---------------------------------------------------------------------------
+# per-segment-restart segmented scan (flag 4): each segment scanned alone
+
+R = oracle.SCAN_SEGMENT_RESTART
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("flags", [0, 1, 2, 3])
+def test_restart_ones_closed_form(dtype, flags):
+    # x = 1: inclusive = 1-based position in the segment, exclusive = 0-based;
+    # reverse counts from the segment's end; segments span several chunks
+    C = oracle.scan_chunk_elems(dtype)
+    lens = [5, 0, 3 * C + 17, 1, C, 40 * C + 3]          # the last one spans anchor intervals
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    x = np.ones(int(off[-1]), dtype)
+    y = oracle.det_segmented_scan(x, off, flags | R)
+    for s_, L in enumerate(lens):
+        p = np.arange(L, dtype=np.float64)
+        if flags & 2:
+            p = p[::-1]
+        want = p + (0 if flags & 1 else 1)
+        assert np.array_equal(y[off[s_]:off[s_ + 1]].astype(np.float64), want)
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+def test_restart_short_segments_are_sequential(dtype):
+    # a segment no longer than one lane is a single lane fold: numpy's cumsum order
+    E = oracle.scan_lane_elems(dtype)
+    rng = np.random.default_rng(35)
+    lens = rng.integers(1, E + 1, 400)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    x = rng.lognormal(0, 1, int(off[-1])).astype(dtype)
+    y = oracle.det_segmented_scan(x, off, R)
+    for s_ in range(lens.size):
+        seg = x[off[s_]:off[s_ + 1]]
+        assert np.array_equal(_bits(y[off[s_]:off[s_ + 1]]), _bits(np.cumsum(seg, dtype=dtype)))
+
+
+def test_restart_differs_from_the_global_grid_reading():
+    # a segment starting at 5 (f32 lanes hold 32 elements): values at segment
+    # positions 0, 30, 60, 90.  Alone, 0 and 30 share lane 0 and position 95 is
+    # ((v0 + v30) + v60) + v90; on the global grid they land in lanes 0, 1, 2, 2
+    # and position 95 (global 100, lane 3) is v0 + (v30 + (v60 + v90)).
+    x = np.full(128, -0.0, np.float32)
+    x[5 + np.array([0, 30, 60, 90])] = [2.0**24, 1.0, 1.0, 1.0]
+    off = np.array([0, 5, 128], np.int64)
+    a = oracle.det_segmented_scan(x, off, R)
+    b = oracle.det_segmented_scan(x, off)
+    assert a[5 + 95] == np.float32(2.0**24)              # (((2^24 + 1) + 1) + 1) rounds to 2^24 each time
+    assert b[5 + 95] == np.float32(2.0**24 + 4)          # 2^24 + 3 rounds to 2^24 + 4
+    one = oracle.det_scan(x[:5])[0], oracle.det_scan(x[5:])[0]
+    assert np.array_equal(_bits(a), _bits(np.concatenate(one)))
+
+
+@pytest.mark.parametrize("flags", [0, 1, 2, 3])
+def test_restart_single_segment_is_the_full_scan(flags):
+    rng = np.random.default_rng(36)
+    x = rng.lognormal(0, 1, 100_003).astype(np.float32)
+    off = np.array([0, x.size], np.int64)
+    assert np.array_equal(_bits(oracle.det_segmented_scan(x, off, flags | R)),
+                          _bits(oracle.det_scan(x, flags)[0]))
