@@ -135,6 +135,7 @@ def build_workload(name, torch, det, dev):
 
     if name.startswith("scan") or name.startswith("segscan"):
         seg = name.startswith("segscan")
+        restart = name == "segscan_restart"
         n = N_OVERRIDE or (workloads.SCAN_SMALL_N if "small" in name else workloads.SCAN_N)
         x_np = workloads.scan_input(n=n, dtype=npdt)
         x = torch.from_numpy(x_np).to(dev)
@@ -147,8 +148,10 @@ def build_workload(name, torch, det, dev):
             off = torch.from_numpy(off_np).to(dev)
             ws = det.workspace(det.lib().det_segmented_scan_workspace_bytes(n, off.numel() - 1, code), dev)
 
+            sflags = det.SCAN_SEGMENT_RESTART if restart else 0
+
             def step():
-                det.det_segmented_scan(x, off, y, workspace=ws, block_threads=BLOCK_THREADS)
+                det.det_segmented_scan(x, off, y, flags=sflags, workspace=ws, block_threads=BLOCK_THREADS)
         else:
             ws = det.workspace(det.lib().det_scan_workspace_bytes(n, code), dev)
 
@@ -165,13 +168,13 @@ def build_workload(name, torch, det, dev):
             m = min(n, 1 << 24)
             if seg:
                 o = workloads.segment_offsets(m)
-                reps, secs = _timed_oracle(lambda: oracle.det_segmented_scan(x_np[:m], o))
+                reps, secs = _timed_oracle(lambda: oracle.det_segmented_scan(x_np[:m], o, 4 if restart else 0))
             else:
                 reps, secs = _timed_oracle(lambda: oracle.det_scan(x_np[:m]))
             return m * reps, secs, f"{reps} x {'segmented ' if seg else ''}scan of the first {m} elements, 1 thread"
 
-        kern = "det_segmented_scan" if seg else "det_scan"
-        extra = " segments geometric(mean 4096)" if seg else ""
+        kern = ("det_segmented_scan_restart" if restart else "det_segmented_scan") if seg else "det_scan"
+        extra = (" segments geometric(mean 4096)" + (", each scanned alone" if restart else "")) if seg else ""
         return dict(state={"x": x, "y": y}, step=step, elems=n, algo_bytes=2 * n * s, step_bytes=2 * n * s,
                     adds=(2 * n) if dt == "f64" else None,
                     dominant=kern,
@@ -679,7 +682,7 @@ def traffic_for(kernel, workload):
 
 OPS = ["sum", "sum_f64", "sum_small", "scatter_f64", "scatter_bin0", "skew", "skew_f32", "scan", "scan_f64",
        "scan_small", "segscan", "rows", "scatter_sub", "scatter_min", "scatter_max", "scan_i32", "slot_alloc",
-       "slot_alloc_multi", "scatter_vec3", "rows_ordered", "gather_grad"]
+       "slot_alloc_multi", "scatter_vec3", "rows_ordered", "gather_grad", "segscan_restart"]
 
 
 def measure_op(name, torch, det, dev, flush, steps, runs, peak):

@@ -33,6 +33,8 @@
 // and all later waits of the launch give up at once.
 #include "det_common.cuh"
 
+#include <algorithm>
+
 namespace det {
 namespace {
 
@@ -821,6 +823,162 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
   }
 }
 
+// Per-segment restart: every segment is scanned as det_scan of the segment
+// alone.  One CTA of 4 warps takes a segment and walks its chunks in order;
+// per chunk the 32 virtual warps of 32 lanes x E elements are handled four at
+// a time, the look-back reads the aggregates of the segment's previous chunks
+// and its interval anchor from shared memory (this CTA computed them), so the
+// association is exactly that of the chunked scan of the segment on its own.
+// A virtual warp's 32 x E elements move between global and shared memory by
+// coalesced warp accesses (any alignment) and reach their lanes from padded
+// rows.
+template <typename T, bool REV, bool EXCL>
+__global__ void __launch_bounds__(128)
+restart_kernel(const T* x, T* y, long long n, const long long* __restrict__ off, long long S,
+               unsigned int* __restrict__ status) {
+  using G = ScanGeom<T>;
+  constexpr int E = G::E, C = G::C, NVW = 32, RS = E + 1;   // RS: padded row stride (conflict-free)
+  __shared__ T stage[4][32 * RS];   // one staging buffer per warp: 32 rows (virtual lanes) of E
+  __shared__ T lx[NVW][32];         // exclusive lane prefixes of the chunk
+  __shared__ T wt[NVW];             // virtual-warp totals
+  __shared__ T wx[NVW];             // exclusive virtual-warp prefixes
+  __shared__ T hist[32];            // aggregates of the segment's last 32 chunks (ring)
+  __shared__ T lastv[NVW];          // exclusive scans: last inclusive value of each virtual warp
+  __shared__ T anchor, excl_s, carry;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  T* st = stage[w];
+  if (blockIdx.x == 0 && tid == 0 && (off[0] != 0 || off[S] != n)) set_status(status, DET_ERR_INVALID_ARG);
+  for (long long sg = blockIdx.x; sg < S; sg += gridDim.x) {
+    const long long o0 = off[sg], o1 = off[sg + 1];
+    if (o1 <= o0) {
+      if (o1 < o0 && tid == 0) set_status(status, DET_ERR_INVALID_ARG);
+      continue;
+    }
+    if (o0 < 0 || o1 > n) {   // invalid offsets: reported, the segment is left alone
+      if (tid == 0) set_status(status, DET_ERR_INVALID_ARG);
+      continue;
+    }
+    const long long len = o1 - o0, nch = (len + C - 1) / C;
+    auto at = [&](long long t) -> long long { return REV ? o1 - 1 - t : o0 + t; };   // scan order -> array index
+    // this warp's virtual warp starting at scan position b: lane l's E elements into v
+    auto load_vw = [&](long long b, T (&v)[E]) {
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        const int idx = i * 32 + lane;   // consecutive lanes on consecutive elements
+        const long long t = b + idx;
+        st[(idx / E) * RS + idx % E] = t < len ? x[at(t)] : absent<T>();
+      }
+      __syncwarp();
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = st[lane * RS + e];
+      __syncwarp();
+    };
+    auto store_vw = [&](long long b, const T (&v)[E]) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) st[lane * RS + e] = v[e];
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        const int idx = i * 32 + lane;
+        const long long t = b + idx;
+        if (t < len) y[at(t)] = st[(idx / E) * RS + idx % E];
+      }
+      __syncwarp();
+    };
+    for (long long k = 0; k < nch; ++k) {
+      // virtual warps of this chunk that hold elements; the others are all
+      // absent, so their totals are -0.0 and change nothing
+      const int nvw = (int)min((long long)NVW, (len - k * C + 32LL * E - 1) / (32LL * E));
+      // ---- phase 1: lane folds, Kogge-Stone over lanes, virtual-warp totals
+      for (int vw = w; vw < nvw; vw += 4) {
+        T v[E];
+        load_vw(k * C + (long long)vw * 32 * E, v);
+        T acc = v[0];
+#pragma unroll
+        for (int e = 1; e < E; ++e) acc = acc + v[e];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const T o = __shfl_up_sync(0xffffffffu, acc, d);
+          if (lane >= d) acc = o + acc;
+        }
+        const T ex = __shfl_up_sync(0xffffffffu, acc, 1);
+        lx[vw][lane] = lane == 0 ? absent<T>() : ex;
+        if (lane == 31) wt[vw] = acc;
+      }
+      __syncthreads();
+      // ---- warp 0: Kogge-Stone over the virtual warps, Agg(k), Excl(k), anchor
+      if (w == 0) {
+        T a = lane < nvw ? wt[lane] : absent<T>();
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const T o = __shfl_up_sync(0xffffffffu, a, d);
+          if (lane >= d) a = o + a;
+        }
+        const T ex = __shfl_up_sync(0xffffffffu, a, 1);
+        wx[lane] = lane == 0 ? absent<T>() : ex;
+        const T agg = __shfl_sync(0xffffffffu, a, 31);
+        const long long K = k / 32;
+        const int j = (int)(k % 32);
+        T v = absent<T>();
+        if (lane < j)
+          v = hist[(k - 1 - lane) & 31];
+        else if (lane == j && K > 0)
+          v = anchor;
+#pragma unroll
+        for (int s2 = 1; s2 < 32; s2 <<= 1) {
+          const T o = __shfl_xor_sync(0xffffffffu, v, s2);
+          v = (lane & s2) ? v + o : o + v;
+        }
+        __syncwarp();   // every lane has read hist and anchor
+        if (lane == 0) {
+          excl_s = v;
+          if (j == 31) anchor = v + agg;   // A(K) = Excl(32K+31) + Agg(32K+31)
+          hist[k & 31] = agg;
+        }
+      }
+      __syncthreads();
+      const T excl = excl_s;
+      // ---- exclusive scans: the last inclusive value of every virtual warp
+      if (EXCL) {
+        for (int vw = w; vw < nvw; vw += 4) {
+          T v[E];
+          load_vw(k * C + (long long)vw * 32 * E, v);
+          if (lane == 31) {
+            T yv = (excl + wx[vw]) + lx[vw][31];
+#pragma unroll
+            for (int e = 0; e < E; ++e) yv = yv + v[e];
+            lastv[vw] = yv;
+          }
+        }
+        __syncthreads();
+      }
+      // ---- phase 2: element values (the chunk is read again, from L2)
+      for (int vw = w; vw < nvw; vw += 4) {
+        const long long b = k * C + (long long)vw * 32 * E;
+        T v[E];
+        load_vw(b, v);
+        T yv = (excl + wx[vw]) + lx[vw][lane];
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          yv = yv + v[e];
+          v[e] = yv;
+        }
+        if (EXCL) {
+          T first = __shfl_up_sync(0xffffffffu, v[E - 1], 1);
+          if (lane == 0) first = vw > 0 ? lastv[vw - 1] : (k > 0 ? carry : T(0.0));
+#pragma unroll
+          for (int e = E - 1; e > 0; --e) v[e] = v[e - 1];
+          v[0] = first;
+        }
+        store_vw(b, v);
+      }
+      __syncthreads();   // shared state is rewritten by the next chunk
+      if (EXCL && tid == 0) carry = lastv[nvw - 1];   // a chunk followed by another is full
+      __syncthreads();
+    }
+  }
+}
+
 // Segment heads in scan order: a bitmap over positions and a per-chunk flag.
 template <int C, bool REV>
 __global__ void seg_heads_kernel(const long long* __restrict__ off, long long nseg, long long n,
@@ -961,6 +1119,23 @@ static int scan_impl(const T* x, T* y, long long n, const long long* seg_off, lo
 
 using namespace det;
 
+template <typename T>
+static int restart_impl(const T* x, T* y, long long n, const long long* off, long long S, int flags, void* ws,
+                        cudaStream_t s) {
+  unsigned int* status = reinterpret_cast<unsigned int*>(ws);
+  const bool rev = flags & DET_SCAN_REVERSE, excl = flags & DET_SCAN_EXCLUSIVE;
+  void (*kern)(const T*, T*, long long, const long long*, long long, unsigned int*) =
+      rev ? (excl ? restart_kernel<T, true, true> : restart_kernel<T, true, false>)
+          : (excl ? restart_kernel<T, false, true> : restart_kernel<T, false, false>);
+  // persistent: one wave of resident CTAs takes the segments in turn
+  const int per_sm = std::max(1, kernel_occupancy((const void*)kern, 128, 0));
+  const long long grid = std::max(1LL, std::min(S, (long long)per_sm * std::max(device_sm_count(), 1)));
+  launch_begin("det_segmented_scan_restart", s);
+  kern<<<(unsigned)grid, 128, 0, s>>>(x, y, n, off, S, status);
+  launch_end(s);
+  return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
+}
+
 extern "C" size_t det_scan_workspace_bytes(int64_t n, int dtype) {
   if (n < 0 || !valid_dtype(dtype)) return 0;
   return dtype == DET_F32 ? scan_ws_layout<float>(n, false).total : scan_ws_layout<double>(n, false).total;
@@ -993,7 +1168,7 @@ extern "C" int det_segmented_scan(const void* x, void* y, int64_t n, const int64
                                   int64_t num_segments, int dtype, int flags, void* workspace,
                                   size_t workspace_bytes, int block_threads, void* stream) {
   if (!valid_dtype(dtype)) return DET_ERR_DTYPE;
-  if (n < 0 || num_segments < 0 || !workspace || (flags & ~3) || !valid_block_threads(block_threads))
+  if (n < 0 || num_segments < 0 || !workspace || (flags & ~7) || !valid_block_threads(block_threads))
     return DET_ERR_INVALID_ARG;
   if (n > 0 && (!x || !y || !seg_offsets || num_segments < 1)) return DET_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % 256) return DET_ERR_WORKSPACE;
@@ -1001,6 +1176,16 @@ extern "C" int det_segmented_scan(const void* x, void* y, int64_t n, const int64
     const char *xb = (const char*)x, *yb = (const char*)y;
     const size_t bytes = (size_t)n * elem_size(dtype);
     if (xb < yb + bytes && yb < xb + bytes) return DET_ERR_INVALID_ARG;
+  }
+  if (flags & DET_SCAN_SEGMENT_RESTART) {
+    if (workspace_bytes < kHeaderBytes) return DET_ERR_WORKSPACE;
+    const cudaStream_t s = as_stream(stream);
+    if (cudaMemsetAsync(workspace, 0, kHeaderBytes, s) != cudaSuccess) return DET_ERR_CUDA;
+    if (n == 0) return DET_OK;
+    return dtype == DET_F32 ? restart_impl<float>((const float*)x, (float*)y, n, (const long long*)seg_offsets,
+                                                  num_segments, flags, workspace, s)
+                            : restart_impl<double>((const double*)x, (double*)y, n, (const long long*)seg_offsets,
+                                                   num_segments, flags, workspace, s);
   }
   if (dtype == DET_F32)
     return scan_impl<float, true>((const float*)x, (float*)y, n, (const long long*)seg_offsets, num_segments,

@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_PKG, "libdet.so")
 F32, F64 = 0, 1
 OK = 0
 SCAN_INCLUSIVE, SCAN_EXCLUSIVE, SCAN_REVERSE = 0, 1, 2
+SCAN_SEGMENT_RESTART = 4   # det_segmented_scan: each segment scanned as det_scan of the segment alone
 SCAN_LANE_ELEMS = {torch.float32: 32, torch.float64: 16}
 SCAN_CHUNK = {torch.float32: 32768, torch.float64: 16384}
 

@@ -60,6 +60,7 @@ extern "C" {
 #define DET_SCAN_INCLUSIVE 0
 #define DET_SCAN_EXCLUSIVE 1
 #define DET_SCAN_REVERSE 2
+#define DET_SCAN_SEGMENT_RESTART 4   /* det_segmented_scan: each segment scanned as det_scan of the segment alone */
 
 /* Frozen scan geometry: a chunk is 32 virtual warps x 32 lanes x E elements,
  * with E = 32 (f32) or 16 (f64); anchor intervals are 32 chunks long. */
@@ -295,6 +296,12 @@ int det_scan(const void* x, void* y, int64_t n, int dtype, int flags, void* tota
  * Segment s is [seg_offsets[s], seg_offsets[s+1]); seg_offsets[0] = 0,
  * seg_offsets[num_segments] = n, non-decreasing (empty segments allowed).
  * Exclusive output is +0.0 at each segment's first element.
+ * With flags | DET_SCAN_SEGMENT_RESTART every segment is instead scanned
+ * exactly as det_scan of the segment alone (its own chunk grid, look-back
+ * and anchors from its first element, scan order); one CTA walks each
+ * segment, so a single very long segment is slow, and in that mode
+ * block_threads is checked and otherwise ignored.  Invalid offsets are
+ * reported through the status word (DET_ERR_INVALID_ARG) in both modes.
  *   seg_offsets device, num_segments + 1 int64
  * Follows: the same pull request, "Validation" (full-array and segmented
  * scans, forward/reverse, inclusive/exclusive).

@@ -251,3 +251,32 @@ def test_rows_ordered_at_bench_size(det):
     det.det_scatter_add_rows(dst, _cuda(idx), _cuda(src), prev_out=prev, ordered=True)
     assert np.array_equal(_bits(dst.cpu().numpy()), _bits(want))
     assert np.array_equal(_bits(prev.cpu().numpy()), _bits(want_prev))
+
+
+# ---------------------------------------------------------------------------
+# per-segment-restart segmented scan
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("flags", [0, 1, 2, 3])
+def test_segmented_scan_restart(det, dtype, flags):
+    C = oracle.scan_chunk_elems(dtype)
+    rng = np.random.default_rng(90 + flags)
+    geo = list(rng.geometric(1 / 4096, 300))
+    lens = [0, 1, 7, 33, C - 1, C, C + 1, 0, 40 * C + 3] + geo + [5]   # empty, lane-sized, chunk edges, anchors
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    x = rng.lognormal(0, 1, int(off[-1])).astype(dtype)
+    want = oracle.det_segmented_scan(x, off, flags | oracle.SCAN_SEGMENT_RESTART)
+    xt = _cuda(x)
+    ot = _cuda(off)
+    got = det.det_segmented_scan(xt, ot, flags=flags | det.SCAN_SEGMENT_RESTART)
+    assert np.array_equal(_bits(got.cpu().numpy()), _bits(want))
+    det.det_segmented_scan(xt, ot, xt, flags=flags | det.SCAN_SEGMENT_RESTART)   # in place
+    assert np.array_equal(_bits(xt.cpu().numpy()), _bits(want))
+
+
+def test_segmented_scan_restart_bench_size(det):
+    x = workloads.scan_input(n=workloads.SCAN_N, dtype=np.float32)
+    off = workloads.segment_offsets(x.size)
+    want = oracle.det_segmented_scan(x, off, oracle.SCAN_SEGMENT_RESTART)
+    got = det.det_segmented_scan(_cuda(x), _cuda(off), flags=det.SCAN_SEGMENT_RESTART)
+    assert np.array_equal(_bits(got.cpu().numpy()), _bits(want))
