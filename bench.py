@@ -133,7 +133,7 @@ def build_workload(name, torch, det, dev):
                     config={"workload": f"det_sum n={n} uniform[0,12) {dt} seed 0", "n": n,
                             "l2": "flushed between timed steps"})
 
-    if name.startswith("scan") or name.startswith("segscan"):
+    if (name.startswith("scan") or name.startswith("segscan")) and name != "scan_i32":
         seg = name.startswith("segscan")
         restart = name == "segscan_restart"
         n = N_OVERRIDE or (workloads.SCAN_SMALL_N if "small" in name else workloads.SCAN_N)
