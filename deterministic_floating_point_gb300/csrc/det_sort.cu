@@ -69,9 +69,9 @@ __device__ __forceinline__ unsigned record_digit(const PassArgs& a, long long i,
 // counts[tile][d] = records of the tile with digit d.  The tile is the
 // scatter pass's tile (K = pass_threads * kIPT records); counting is
 // order-free, so here each thread simply streams its share of the tile with
-// 16-byte loads, several in flight, and adds one shared atomic per record
-// (records sharing lane 0's digit are added by one atomic, so a hot digit
-// does not serialise on one address).
+// 16-byte loads, several in flight, and keeps a run of equal digits in
+// registers, adding it by one shared atomic when the digit changes (a hot
+// digit costs almost no atomics).
 template <bool FIRST>
 __global__ void __launch_bounds__(256, 8) sort_count_kernel(PassArgs a, long long K) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -84,6 +84,9 @@ __global__ void __launch_bounds__(256, 8) sort_count_kernel(PassArgs a, long lon
   for (int d = tid; d < ndig; d += blockDim.x) cnt[d] = 0u;
   __syncthreads();
   const long long t0 = tile * K, t1 = min(N, t0 + K);
+  // a run of equal digits is kept in registers and added by one atomic when
+  // the digit changes (records are counted in any order)
+  unsigned rd = 0xffffffffu, rc = 0;
   auto count = [&](int k, bool in) {
     unsigned d = 0xffffffffu;
     if (in) {
@@ -98,12 +101,13 @@ __global__ void __launch_bounds__(256, 8) sort_count_kernel(PassArgs a, long lon
         d = ((unsigned)k >> a.shift) & mask;
       }
     }
-    const bool valid = d != 0xffffffffu;
-    const unsigned d0 = __shfl_sync(0xffffffffu, d, 0);
-    const unsigned same0 = __ballot_sync(0xffffffffu, valid && d == d0);
-    // lane 0 adds its whole digit group; the other lanes add themselves (if
-    // lane 0 is invalid, d0 matches no valid digit)
-    if (valid && (d != d0 || lane == 0)) atomicAdd(&cnt[d], d == d0 ? (unsigned)__popc(same0) : 1u);
+    if (d == 0xffffffffu) return;
+    if (d != rd) {
+      if (rc) atomicAdd(&cnt[rd], rc);
+      rd = d;
+      rc = 0;
+    }
+    ++rc;
   };
   if (t0 < t1) {
     const bool vec = (reinterpret_cast<uintptr_t>(a.keys_in + t0) & 15) == 0;
@@ -131,6 +135,7 @@ __global__ void __launch_bounds__(256, 8) sort_count_kernel(PassArgs a, long lon
       count(j < t1 ? __ldg(a.keys_in + j) : 0, j < t1);
     }
   }
+  if (rc) atomicAdd(&cnt[rd], rc);
   __syncthreads();
   for (int d = tid; d < ndig; d += blockDim.x) a.counts[tile * ndig + d] = cnt[d];
 }
