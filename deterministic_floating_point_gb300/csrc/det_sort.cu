@@ -759,7 +759,9 @@ SortPlan make_sort_plan(long long n, long long m, int value_bytes, bool need_idx
   }
   p.seg = off;
   off = align_up(off + (size_t)(m + 1) * 4, 256);
-  p.max_blocks = 2 * (n / kSegBlock) + 2;
+  // blocks of long bins: ceil(len / 2048) <= len / 2048 + 1 each, and at most
+  // min(m, n / 2048) bins are long (each holds more than 2048 records)
+  p.max_blocks = n / kSegBlock + std::min(m, n / kSegBlock) + 2;
   p.max_lsegs = n / kSegBlock + 2;
   p.blocks = off;
   off = align_up(off + (size_t)p.max_blocks * 8, 256);
