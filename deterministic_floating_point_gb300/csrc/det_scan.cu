@@ -537,6 +537,10 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
     for (int i = tid; i < C / 32; i += 1024) sm.heads[hb][i] = (w0 + i < nwords) ? a.head_bits[w0 + i] : 0u;
   };
   auto head_of = [&](int hb, int t) -> bool { return SEG && ((sm.heads[hb][t >> 5] >> (t & 31)) & 1u); };
+  // this lane's E head bits (bit e: position t0 + e), read once: E divides 32
+  auto lane_heads = [&](int hb) -> unsigned {
+    return SEG ? (sm.heads[hb][t0 >> 5] >> (t0 & 31)) & (E == 32 ? 0xffffffffu : ((1u << E) - 1u)) : 0u;
+  };
 
   // Phase 1 after the lane fold: Kogge-Stone over lanes (-> lx), then over
   // warps by warp 0 (-> wx[set]) and publication of Agg(c).  Ends with the
@@ -622,11 +626,12 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
   __syncthreads();
   {
     T acc = x[0];
-    bool f = head_of(hb, t0);
+    const unsigned hw = lane_heads(hb);
+    bool f = hw & 1u;
 #pragma unroll
     for (int e = 1; e < E; ++e) {
       bool fr;
-      segop<T, SEG>(f, acc, head_of(hb, t0 + e), x[e], fr, acc);
+      segop<T, SEG>(f, acc, (hw >> e) & 1u, x[e], fr, acc);
       f = fr;
     }
     finish_phase1(acc, f, set, c, lx, lxf);
@@ -692,6 +697,7 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
       __syncthreads();
       T acc = absent<T>();
       bool f = false;
+      const unsigned hwn = lane_heads(hb ^ 1);
       if (next_staged) {
         const T* row = stage + tid * ROW;
 #pragma unroll
@@ -705,10 +711,10 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
             const T xe = REV ? pv[PER16 - 1 - k] : pv[k];
             if (e == 0) {
               acc = xe;
-              f = head_of(hb ^ 1, t0);
+              f = hwn & 1u;
             } else {
               bool fr;
-              segop<T, SEG>(f, acc, head_of(hb ^ 1, t0 + e), xe, fr, acc);
+              segop<T, SEG>(f, acc, (hwn >> e) & 1u, xe, fr, acc);
               f = fr;
             }
           }
@@ -720,10 +726,10 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
           const T xe = t < a.n ? a.x[gidx(cn, t0 + e)] : absent<T>();
           if (e == 0) {
             acc = xe;
-            f = head_of(hb ^ 1, t0);
+            f = hwn & 1u;
           } else {
             bool fr;
-            segop<T, SEG>(f, acc, head_of(hb ^ 1, t0 + e), xe, fr, acc);
+            segop<T, SEG>(f, acc, (hwn >> e) & 1u, xe, fr, acc);
             f = fr;
           }
         }
@@ -741,9 +747,10 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
       T y;
       segop<T, SEG>(SEG && sm.exclf, sm.excl, SEG && ((sm.wxf[set] >> w) & 1u), sm.wx[set][w], f1, y);
       segop<T, SEG>(f1, y, lxf, lx, f2, y);
+      const unsigned hw = lane_heads(hb);
 #pragma unroll
       for (int e = 0; e < E; ++e) {
-        y = (SEG && head_of(hb, t0 + e)) ? x[e] : y + x[e];
+        y = (SEG && ((hw >> e) & 1u)) ? x[e] : y + x[e];
         x[e] = y;
       }
     }
@@ -765,8 +772,10 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
       __syncthreads();
       if (lane == 0) pl = (w > 0) ? sm.last[w - 1] : T(0.0);   // chunk start: written later
 #pragma unroll
-      for (int e = E - 1; e > 0; --e) x[e] = (SEG && head_of(hb, t0 + e)) ? T(0.0) : x[e - 1];
-      x[0] = (SEG && head_of(hb, t0)) ? T(0.0) : pl;
+      const unsigned hw = lane_heads(hb);
+#pragma unroll
+      for (int e = E - 1; e > 0; --e) x[e] = (SEG && ((hw >> e) & 1u)) ? T(0.0) : x[e - 1];
+      x[0] = (SEG && (hw & 1u)) ? T(0.0) : pl;
     }
     {
       const long long g0 = REV ? a.n - base - t0 - E : base + t0;
