@@ -2,6 +2,7 @@
 #include "det_common.cuh"
 
 #include <atomic>
+#include <cstdio>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -40,11 +41,26 @@ int cached_attr(std::atomic<int>* cache, cudaDeviceAttr attr) {
 }
 }  // namespace
 
+namespace {
+std::mutex g_err_mu;
+char g_err[256] = "";
+}  // namespace
+
+int cuda_fail(cudaError_t e, const char* where) {
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  snprintf(g_err, sizeof(g_err), "%s: %s", where, cudaGetErrorName(e));
+  return DET_ERR_CUDA;
+}
+
+const char* last_cuda_error() { return g_err; }
+
 int device_sm_count() { return cached_attr(g_sms, cudaDevAttrMultiProcessorCount); }
 int device_max_smem_optin() { return cached_attr(g_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin); }
 
 cudaError_t ensure_dyn_smem(const void* kernel, size_t bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;   // within the default limit
+  // within the default limit even with a kernel's static shared arrays (the
+  // 48 KB default covers static + dynamic bytes)
+  if (bytes <= 32 * 1024) return cudaSuccess;
   int dev = 0;
   cudaGetDevice(&dev);
   std::lock_guard<std::mutex> lk(g_dyn_mu);
@@ -109,6 +125,8 @@ extern "C" int det_read_status(const void* workspace, void* stream, int* device_
   *device_status = (int)v;
   return DET_OK;
 }
+
+extern "C" const char* det_last_cuda_error(void) { return det::last_cuda_error(); }
 
 extern "C" const char* det_status_string(int status) {
   switch (status) {

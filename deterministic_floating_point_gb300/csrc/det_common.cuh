@@ -184,6 +184,14 @@ __device__ __forceinline__ void ld_acquire_v2u64(const unsigned long long* p, un
 }
 
 // Record a device-detected error in the status word (first error wins).
+// Record a failed CUDA call (`where` = the step) for det_last_cuda_error and
+// return DET_ERR_CUDA.  check_launch does the same for the last launch.
+int cuda_fail(cudaError_t e, const char* where);
+inline int check_launch(const char* where) {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DET_OK : cuda_fail(e, where);
+}
+
 __device__ __forceinline__ void set_status(unsigned int* status, unsigned int code) {
   atomicCAS(status, 0u, code);
 }

@@ -846,7 +846,8 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
     launch_begin("det_sort_colscan", s);
     sort_colscan_kernel<<<(unsigned)((ndig + kColDigits - 1) / kColDigits), 1024, 0, s>>>(a, first ? 1 : 0);
     launch_end(s);
-    if (cudaGetLastError() != cudaSuccess) return DET_ERR_CUDA;
+    const int rc = check_launch("sort: digit counts");
+    if (rc != DET_OK) return rc;
     const bool keys_out = p.passes > 1;
     cudaError_t e;
     if (p.value_bytes == 8)
@@ -855,7 +856,7 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
       e = launch_pass<4>(a, first, p.need_idx, keys_out, p.threads, p.tiles, s);
     else
       e = launch_pass<0>(a, first, p.need_idx, keys_out, p.threads, p.tiles, s);
-    if (e != cudaSuccess) return DET_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_fail(e, "sort: pass");
   }
   if (p.passes > 1) {   // one-pass sorts got their segment starts from the pass
     launch_begin("det_sort_bounds", s);
@@ -863,7 +864,7 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
         reinterpret_cast<const int32_t*>(w + p.keys[*final_buf]), &h->n_valid, p.m, seg, p.n);
     launch_end(s);
   }
-  return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
+  return check_launch("sort: segment starts");
 }
 
 template <typename T>
@@ -885,12 +886,14 @@ int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T*
                                                          &h->long_blocks, &h->long_segs, &h->n_valid, p.max_blocks,
                                                          p.max_lsegs, &h->status, ostride);
   launch_end(s);
+  const int rc = check_launch("segmented tree: bins");
+  if (rc != DET_OK) return rc;
   launch_begin("det_segtree_blocks", s);
   auto* kk = negate ? segtree_blocks_kernel<T, true> : segtree_blocks_kernel<T, false>;
   kk<<<(unsigned)p.max_blocks, 256, 0, s>>>(sorted_vals, seg, blocks, &h->long_blocks, lsegs, ldone, nodes, out,
                                             &h->n_valid, p.max_blocks, p.max_lsegs, ostride);
   launch_end(s);
-  return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
+  return check_launch("segmented tree: blocks");
 }
 
 template int enqueue_segmented_tree<float>(const SortPlan&, void*, const float*, float*, cudaStream_t, bool, long long,

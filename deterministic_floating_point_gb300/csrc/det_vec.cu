@@ -53,7 +53,8 @@ int vec_impl(T* out, long long m, long long width, const int32_t* bins, const T*
   char* w = reinterpret_cast<char*>(ws);
   SortHdr* h = reinterpret_cast<SortHdr*>(ws);
   T* comp = reinterpret_cast<T*>(w + L.comp);
-  const long long grid = std::max(1LL, std::min((n + 255) / 256, 8LL * std::max(device_sm_count(), 1)));
+  // one thread per record: many independent gathers in flight
+  const long long grid = std::max(1LL, (long long)((n + 255) / 256));
   launch_begin("det_vec_gather", s);
   vec_gather_kernel<T><<<(unsigned)grid, 256, 0, s>>>(values, width, reinterpret_cast<const int32_t*>(w + p.idx[fb]),
                                                        &h->n_valid, n, comp);

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libdet.so")
 
 F32, F64 = 0, 1
 OK = 0
+ERR_CUDA = 6   # DET_ERR_CUDA: a CUDA call or launch failed (detail: det_last_cuda_error)
 SCAN_INCLUSIVE, SCAN_EXCLUSIVE, SCAN_REVERSE = 0, 1, 2
 SCAN_SEGMENT_RESTART = 4   # det_segmented_scan: each segment scanned as det_scan of the segment alone
 SCAN_LANE_ELEMS = {torch.float32: 32, torch.float64: 16}
@@ -55,6 +56,7 @@ _SIGNATURES = {
     "det_slot_alloc": (_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _sz, _int, _vp]),
     "det_read_status": (_int, [_vp, _vp, ctypes.POINTER(_int)]),
     "det_status_string": (ctypes.c_char_p, [_int]),
+    "det_last_cuda_error": (ctypes.c_char_p, []),
     "det_profile_set_events": (_int, [_vp, _int]),
     "det_profile_event_count": (_int, []),
     "det_profile_event_name": (ctypes.c_char_p, [_int]),
@@ -71,7 +73,13 @@ _SIGNATURES = {
 class DetError(RuntimeError):
     def __init__(self, code: int, what: str):
         self.code = code
-        super().__init__(f"{what}: {status_string(code)} (code {code})")
+        detail = ""
+        if code == ERR_CUDA:
+            try:
+                detail = " [" + lib().det_last_cuda_error().decode() + "]"
+            except Exception:  # pragma: no cover - only when the library is absent
+                pass
+        super().__init__(f"{what}: {status_string(code)} (code {code}){detail}")
 
 
 def lib():

@@ -369,6 +369,12 @@ int det_slot_alloc(int32_t* counter, int64_t num_counters, const int32_t* index,
 int det_read_status(const void* workspace, void* stream, int* device_status);
 const char* det_status_string(int status);
 
+/* The last CUDA failure a call of this library met (the step that failed and
+ * the CUDA error name), or "" if none: the detail behind DET_ERR_CUDA.  The
+ * string lives in library storage until the next failure; calls on other
+ * threads may replace it. */
+const char* det_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif
