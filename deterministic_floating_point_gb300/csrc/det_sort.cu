@@ -1,29 +1,29 @@
 // Stable LSD radix sort of (key, value, index) records with a validity
 // filter, and the segmented pairwise tree over the sorted values.
 //
-//   count p   per tile of K = threads * 32 records: digit counts of the
+//   count p   per tile of K = threads * 16 records: digit counts of the
 //             valid records (shared integer atomics: order-free)
 //   colscan p per digit: exclusive prefix of the counts over tiles, and the
 //             digit totals (pass 0 also sums them into the valid count)
-//   pass p    per tile, independently: digit starts from the totals; a warp
-//             multi-split (peer masks OR-ed into per-warp shared words) and
-//             per-warp shared counters give each record its rank among
-//             earlier records of its digit inside the warp; position = digit
-//             start + tile prefix + warp prefix + rank.
+//   pass p    per tile, independently: a stable sort of the tile's records
+//             by digit in shared memory (one or two counting sub-passes of
+//             32 buckets), then record p of that order goes to
+//             digit start + tile prefix + (p - tile-local digit start).
 //             Records keep their input order inside a digit: the pass is
 //             stable, so after the last pass each destination's records are
 //             in ascending original index.
 //   bounds    (more than one pass) segment starts from the sorted keys
-//   tree      out[b] = out[b] + PT(group b): groups of at most 2048 records
-//             are reduced by one warp; longer groups are cut into
-//             rank-aligned 2048-blocks (subtrees of the group's tree),
-//             reduced by one warp each, then a tree over the block nodes.
+//   tree      out[b] = out[b] + PT(group b): groups of at most 32 records
+//             by one thread, of at most 1024 by one warp; longer groups are
+//             cut into rank-aligned 4096-blocks (subtrees of the group's
+//             tree), reduced by one CTA each, then a tree over the block
+//             nodes.
 #include "det_sort.cuh"
 
 namespace det {
 namespace {
 
-constexpr int kIPT = 32;                 // records per thread per tile
+constexpr int kIPT = 16;                 // records per thread of a pass
 // ---------------------------------------------------------------------------
 struct PassArgs {
   const int32_t* keys_in;
@@ -67,75 +67,72 @@ __device__ __forceinline__ unsigned record_digit(const PassArgs& a, long long i,
 }
 
 // counts[tile][d] = records of the tile with digit d.  The tile is the
-// scatter pass's tile (K = pass_threads * kIPT records); counting is
-// order-free, so here each thread simply streams its share of the tile with
-// 16-byte loads, several in flight, and keeps a run of equal digits in
-// registers, adding it by one shared atomic when the digit changes (a hot
-// digit costs almost no atomics).
+// scatter pass's tile (K = pass_threads * kIPT records).  A full, aligned
+// tile's keys come in by one bulk copy into shared memory (32 KB in flight
+// per CTA); counting is order-free, so each thread then adds its keys by
+// shared atomics (dropped keys into a spare slot).  A group of four keys
+// that is one digit across the whole warp is added by lane 0 alone: a hot
+// digit would otherwise serialise the warp's atomics on one address.
 template <bool FIRST>
-__global__ void __launch_bounds__(256, 8) sort_count_kernel(PassArgs a, long long K) {
+__global__ void __launch_bounds__(256) sort_count_kernel(PassArgs a, long long K) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  unsigned int* cnt = reinterpret_cast<unsigned int*>(smem_raw);   // [ndig]
-  const int tid = threadIdx.x, lane = tid & 31;
+  __shared__ __align__(8) unsigned long long keys_bar;
   const int ndig = 1 << a.D;
+  unsigned int* cnt = reinterpret_cast<unsigned int*>(smem_raw);   // [ndig + 1]; ndig = dropped
+  int32_t* skeys = reinterpret_cast<int32_t*>(smem_raw + align_up((size_t)(ndig + 1) * 4, 16));   // [K]
+  const int tid = threadIdx.x, lane = tid & 31;
   const unsigned mask = (unsigned)ndig - 1u;
   const long long tile = blockIdx.x;
   const long long N = FIRST ? a.n : (long long)*a.n_valid;
-  for (int d = tid; d < ndig; d += blockDim.x) cnt[d] = 0u;
-  __syncthreads();
   const long long t0 = tile * K, t1 = min(N, t0 + K);
-  // a run of equal digits is kept in registers and added by one atomic when
-  // the digit changes (records are counted in any order)
-  unsigned rd = 0xffffffffu, rc = 0;
-  auto count = [&](int k, bool in) {
-    unsigned d = 0xffffffffu;
-    if (in) {
-      if (FIRST) {
-        if (a.key_offset == 0) {
-          if ((unsigned)k < (unsigned long long)a.m) d = ((unsigned)k >> a.shift) & mask;
-        } else {
-          const long long kk = (long long)k + a.key_offset;
-          if (kk >= 0 && kk < a.m) d = ((unsigned)kk >> a.shift) & mask;
-        }
-      } else {
-        d = ((unsigned)k >> a.shift) & mask;
-      }
-    }
-    if (d == 0xffffffffu) return;
-    if (d != rd) {
-      if (rc) atomicAdd(&cnt[rd], rc);
-      rd = d;
-      rc = 0;
-    }
-    ++rc;
-  };
-  if (t0 < t1) {
-    const bool vec = (reinterpret_cast<uintptr_t>(a.keys_in + t0) & 15) == 0;
-    constexpr int U = 4;   // 16-byte loads in flight per thread per step
-    long long i = t0;
-    if (vec) {
-      const long long span = (long long)blockDim.x * 4 * U;
-      for (; i + span <= t1; i += span) {
-        int4 q[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          q[u] = __ldg(reinterpret_cast<const int4*>(a.keys_in + i + (long long)u * blockDim.x * 4) + tid);
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          count(q[u].x, true);
-          count(q[u].y, true);
-          count(q[u].z, true);
-          count(q[u].w, true);
-        }
-      }
-    }
-    // remainder: whole warps step together, lanes past the end count nothing
-    for (long long b = i + (long long)(tid & ~31); b < t1; b += blockDim.x) {
-      const long long j = b + lane;
-      count(j < t1 ? __ldg(a.keys_in + j) : 0, j < t1);
-    }
+  const bool bulk = t1 - t0 == K && (reinterpret_cast<uintptr_t>(a.keys_in + t0) & 15) == 0;
+  if (bulk && tid == 0) {
+    mbar_init(&keys_bar, 1);
+    mbar_arrive_expect_tx(&keys_bar, (unsigned)(K * 4));
+    bulk_copy_g2s(skeys, a.keys_in + t0, (unsigned)(K * 4), &keys_bar);
   }
-  if (rc) atomicAdd(&cnt[rd], rc);
+  for (int d = tid; d <= ndig; d += blockDim.x) cnt[d] = 0u;
+  __syncthreads();
+  const bool plain = !FIRST || a.key_offset == 0;
+  const unsigned m32 = (unsigned)min(a.m, (long long)0x80000000LL);   // keys are int32
+  const int shift = a.shift;
+  auto digit = [&](int k) -> unsigned {
+    if (FIRST) {
+      if (plain) return (unsigned)k < m32 ? ((unsigned)k >> shift) & mask : (unsigned)ndig;
+      const long long kk = (long long)k + a.key_offset;
+      return (kk >= 0 && kk < a.m) ? ((unsigned)kk >> shift) & mask : (unsigned)ndig;
+    }
+    return ((unsigned)k >> shift) & mask;
+  };
+  if (bulk) {
+    const bool ok = mbar_wait(&keys_bar, 0, kWaitNs);
+    if (__syncthreads_or(!ok)) {
+      // the copy did not complete: record it, give it (bounded) time to land, leave
+      if (tid == 0) {
+        set_status(a.status, DET_ERR_COPY_TIMEOUT);
+        mbar_wait(&keys_bar, 0, kWaitNs);
+      }
+      __syncthreads();
+      return;
+    }
+    const int4* k4 = reinterpret_cast<const int4*>(skeys);
+#pragma unroll 4
+    for (int g = tid; g < (int)(K / 4); g += blockDim.x) {
+      const int4 q = k4[g];
+      const unsigned d0 = digit(q.x), d1 = digit(q.y), d2 = digit(q.z), d3 = digit(q.w);
+      const unsigned w0 = __shfl_sync(0xffffffffu, d0, 0);
+      if (__all_sync(0xffffffffu, d0 == w0 && d1 == w0 && d2 == w0 && d3 == w0)) {
+        if (lane == 0) atomicAdd(&cnt[w0], 128u);
+      } else {
+        atomicAdd(&cnt[d0], 1u);
+        atomicAdd(&cnt[d1], 1u);
+        atomicAdd(&cnt[d2], 1u);
+        atomicAdd(&cnt[d3], 1u);
+      }
+    }
+  } else {
+    for (long long j = t0 + tid; j < t1; j += blockDim.x) atomicAdd(&cnt[digit(__ldg(a.keys_in + j))], 1u);
+  }
   __syncthreads();
   for (int d = tid; d < ndig; d += blockDim.x) a.counts[tile * ndig + d] = cnt[d];
 }
@@ -153,9 +150,17 @@ __global__ void __launch_bounds__(1024) sort_colscan_kernel(PassArgs a, int coun
   const long long T = a.tiles;
   const long long TG = (T + kColGroups - 1) / kColGroups;
   const long long t0 = g * TG, t1 = min(T, t0 + TG);
+  // the tiles of a group are read eight at a time (independent loads in flight)
+  constexpr int kU = 8;
   unsigned sum = 0;
   if (d < ndig)
-    for (long long t = t0; t < t1; ++t) sum += a.counts[t * ndig + d];
+    for (long long t = t0; t < t1; t += kU) {
+      unsigned v[kU];
+#pragma unroll
+      for (int k = 0; k < kU; ++k) v[k] = t + k < t1 ? a.counts[(t + k) * ndig + d] : 0u;
+#pragma unroll
+      for (int k = 0; k < kU; ++k) sum += v[k];
+    }
   part[g][dl] = sum;
   __syncthreads();
   if (warp < kColDigits) {
@@ -183,16 +188,22 @@ __global__ void __launch_bounds__(1024) sort_colscan_kernel(PassArgs a, int coun
     const int dc = blockIdx.x * kColDigits + c;
     if (lane == 0 && dc < ndig) {
       a.totals[dc] = total;
+      a.counts[T * ndig + dc] = total;   // row `tiles`: the pass takes a tile's counts as E[t + 1] - E[t]
       if (count_valid && total) atomicAdd(a.n_valid, total);
     }
   }
   __syncthreads();
   unsigned run = part[g][dl];
   if (d < ndig)
-    for (long long t = t0; t < t1; ++t) {
-      const unsigned v = a.counts[t * ndig + d];
-      a.counts[t * ndig + d] = run;
-      run += v;
+    for (long long t = t0; t < t1; t += kU) {
+      unsigned v[kU];
+#pragma unroll
+      for (int k = 0; k < kU; ++k) v[k] = t + k < t1 ? a.counts[(t + k) * ndig + d] : 0u;
+#pragma unroll
+      for (int k = 0; k < kU; ++k) {
+        if (t + k < t1) a.counts[(t + k) * ndig + d] = run;
+        run += v[k];
+      }
     }
 }
 
@@ -236,346 +247,381 @@ __device__ __forceinline__ void digit_starts(const unsigned int* totals, int ndi
   __syncthreads();
 }
 
-// 4- or 8-byte asynchronous copy global -> shared (both naturally aligned).
-template <int BYTES>
-__device__ __forceinline__ void cp_async_small(void* smem, const void* gmem) {
-  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(sa), "l"(gmem), "n"(BYTES) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
-}
+// ---------------------------------------------------------------------------
+// The scatter pass.  Inside a tile the records are ranked by a stable sort in
+// shared memory; record p of the tile's sorted order then goes to
+//   digit start + earlier tiles' records of its digit + (p - the tile-local
+//   start of its digit)
+// and consecutive p of one digit land on consecutive positions.
+//
+// The tile's valid records are sorted by digit with one or two stable
+// counting sub-passes of 32 buckets (the low 5 bits, then the rest; one
+// sub-pass for digits of at most 5 bits).  In a sub-pass thread t holds the
+// 16 consecutive records [16t, 16t + 16) of the current order:
+//   walk 1  count its records per bucket in its own counter column
+//   scan    exclusive scan of all counters, bucket-major, thread-minor
+//   walk 2  rank = its scanned counter, post-incremented, in record order
+// so equal buckets keep thread order and, inside a thread, record order: the
+// sub-pass is stable, and so is the sort.  Dropped records (past the end,
+// or a destination outside [0, m)) carry a flag; the last sub-pass neither
+// counts nor places them, so the valid records take ranks [0, valid count).
+// Counters are the 16-bit halves of 32-bit words: word (row r, thread t) at
+// r * T + t counts bucket r (low half) and bucket r + 16 (high half), so a
+// warp's counter accesses never share a bank.
+// Records live in shared memory as 32-bit words (flag << 31 | digit << 13 |
+// tile-local index) under an XOR swizzle of the 16-byte chunks in each
+// 128-byte line, so that the per-thread row reads are conflict-free.
+constexpr int kIdxBits = 13;          // tile-local record index (tiles of at most 8,192 records)
+constexpr unsigned kDropped = 1u << 31;
 
 template <int VB> struct Payload;
 template <> struct Payload<0> { using U = unsigned int; };
 template <> struct Payload<4> { using U = unsigned int; };
 template <> struct Payload<8> { using U = unsigned long long; };
 
-// Shared bytes of the staging area of a pass (records in tile-sorted order).
-__host__ __device__ inline size_t pass_staging_bytes(long long K, int vb, bool idx, bool keys_out) {
-  return (size_t)K * (vb + (idx ? 4 : 0) + (keys_out ? 4 : 0) + 2);
-}
-__host__ __device__ inline size_t pass_front_bytes(int nwarps, int ndig, long long K, int vb, bool idx, bool keys_out,
-                                                   bool stage) {
-  const size_t ranking = (size_t)nwarps * ndig * 6;
-  const size_t staging = stage ? pass_staging_bytes(K, vb, idx, keys_out) : 0;
-  return align_up(ranking > staging ? ranking : staging, 16);
+// Physical word of logical record position p.  With kSwizzle the 16-byte
+// chunks of each 128-byte line are XOR-permuted by the line index (an
+// involution), which makes the per-thread row reads conflict-free; without
+// it those reads take four wavefronts per phase (measured slower overall).
+constexpr bool kSwizzle = true;
+__device__ __forceinline__ unsigned swz(unsigned p) { return kSwizzle ? p ^ (((p >> 5) & 7u) << 2) : p; }
+
+// Shared-memory layout of a pass (bytes; every part 16-byte aligned).
+struct PassSmem {
+  size_t recs, rkeys, vals, idx, cnt, off, total;
+};
+__host__ __device__ inline PassSmem pass_smem(int T, int ndig, int vb, bool idx_in, bool keys_out) {
+  const size_t K = (size_t)T * kIPT;
+  PassSmem s;
+  size_t o = 0;
+  s.recs = o;
+  o += K * 4;
+  s.rkeys = o;   // raw keys, kept apart from the records only when they are written out
+  o += keys_out ? K * 4 : 0;
+  s.vals = o;
+  o += K * (size_t)vb;
+  s.idx = o;
+  o += idx_in ? K * 4 : 0;
+  s.cnt = o;
+  o += (size_t)17 * T * 4;   // 16 counter rows and a spare row for dropped records
+  s.off = o;
+  o += align_up((size_t)(ndig + 1) * 4, 16);
+  s.total = o;
+  return s;
 }
 
-template <int VB, bool FIRST, bool IDX, bool KEYS_OUT, bool STAGE>
-__global__ void __launch_bounds__(256, 3) sort_pass_kernel(PassArgs a) {
+// Exclusive scan of one value per thread over the CTA in thread order;
+// *total receives the sum.  wsum: 32 words of shared memory.  Ends with a
+// barrier, so wsum can be reused at once.
+__device__ __forceinline__ unsigned block_excl_scan(unsigned v, unsigned* wsum, unsigned* total) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  unsigned x = v;
+#pragma unroll
+  for (int s = 1; s < 32; s <<= 1) {
+    const unsigned o = __shfl_up_sync(0xffffffffu, x, s);
+    if (lane >= s) x += o;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned wv = lane < nw ? wsum[lane] : 0u;
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+      const unsigned o = __shfl_up_sync(0xffffffffu, wv, s);
+      if (lane >= s) wv += o;
+    }
+    wsum[lane] = wv;
+  }
+  __syncthreads();
+  const unsigned pre = (warp ? wsum[warp - 1] : 0u) + x - v;
+  *total = wsum[nw - 1];
+  __syncthreads();
+  return pre;
+}
+
+// This thread's row of records: logical positions [16t, 16t + 16).
+__device__ __forceinline__ void load_row(unsigned (&rec)[kIPT], const unsigned* recs) {
+  const int tid = threadIdx.x;
+  const uint4* q4 = reinterpret_cast<const uint4*>(recs);
+  const unsigned g0 = 4u * tid, x = kSwizzle ? (g0 >> 3) & 7u : 0u;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 q = q4[(g0 + c) ^ x];
+    rec[4 * c] = q.x;
+    rec[4 * c + 1] = q.y;
+    rec[4 * c + 2] = q.z;
+    rec[4 * c + 3] = q.w;
+  }
+}
+
+// One stable counting sub-pass by bucket (rec >> S) & 31.  LAST: dropped
+// records are left out -- counted in a spare row 16 that the scan skips,
+// and "placed" on that row's word, so every record takes the same
+// branch-free steps.  The ranked records are written to `recs` in the new
+// order; unless LAST, rec[] then holds this thread's row of it.
+template <int S, bool LAST>
+__device__ __forceinline__ void rank_subpass(unsigned (&rec)[kIPT], unsigned* __restrict__ recs,
+                                             unsigned* __restrict__ cnt, unsigned* wsum) {
+  const int T = blockDim.x, tid = threadIdx.x;
+  unsigned* col = cnt + tid;
+  unsigned* spare = col + 16 * T;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) col[r * T] = 0u;
+#pragma unroll
+  for (int j = 0; j < kIPT; ++j) {
+    const unsigned b = (rec[j] >> S) & 31u;
+    unsigned* w = col + (b & 15u) * T;
+    if (LAST) w = (rec[j] & kDropped) ? spare : w;
+    *w += 1u << (b & 16u);
+  }
+  __syncthreads();
+  // scan: thread t takes the words [16t, 16t + 16) of the row-major counter
+  // matrix; the low halves (buckets < 16) all come before the high halves
+  uint4* run = reinterpret_cast<uint4*>(cnt) + 4 * tid;
+  uint4 v[4];
+  unsigned sum = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    v[c] = run[c];
+    sum += v[c].x + v[c].y + v[c].z + v[c].w;
+  }
+  unsigned tot;
+  unsigned pre = block_excl_scan(sum, wsum, &tot);
+  pre += (tot & 0xffffu) << 16;   // halves never carry: every count is at most 8,192
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 o;
+    o.x = pre;
+    pre += v[c].x;
+    o.y = pre;
+    pre += v[c].y;
+    o.z = pre;
+    pre += v[c].z;
+    o.w = pre;
+    pre += v[c].w;
+    run[c] = o;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kIPT; ++j) {
+    const unsigned b = (rec[j] >> S) & 31u;
+    const bool drop = LAST && (rec[j] & kDropped);
+    unsigned* w = drop ? spare : col + (b & 15u) * T;
+    const unsigned x = *w;
+    *w = x + (1u << (b & 16u));
+    unsigned* dst = recs + swz((x >> (b & 16u)) & 0xffffu);
+    *(drop ? spare : dst) = rec[j];
+  }
+  __syncthreads();
+  if (!LAST) load_row(rec, recs);
+}
+
+template <int VB, bool FIRST, bool IDX, bool KEYS_OUT>
+__global__ void __launch_bounds__(512, 2) sort_pass_kernel(PassArgs a) {
   using U = typename Payload<VB>::U;
+  constexpr bool IDX_IN = IDX && !FIRST;                // input indices carried from the previous pass
+  constexpr bool RANK = VB == 0 && !IDX && !KEYS_OUT;   // only each record's sorted position is wanted
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  __shared__ unsigned int wsum[32];
+  __shared__ __align__(8) unsigned long long pay_bar;
+  const int T = blockDim.x, tid = threadIdx.x;
   const int ndig = 1 << a.D;
   const unsigned mask = (unsigned)ndig - 1u;
-  unsigned int* pmask = reinterpret_cast<unsigned int*>(smem_raw);                           // [nwarps][ndig]
-  unsigned short* wcnt = reinterpret_cast<unsigned short*>(smem_raw + (size_t)nwarps * ndig * 4); // [nwarps][ndig]
-  unsigned int* gbase = reinterpret_cast<unsigned int*>(
-      smem_raw + pass_front_bytes(nwarps, ndig, a.K, VB, IDX, KEYS_OUT, STAGE));   // [ndig + 1]
-  __shared__ unsigned int wsum[32];
-  __shared__ unsigned int n_digits;   // distinct digits of the tile
+  const PassSmem L = pass_smem(T, ndig, VB, IDX_IN, KEYS_OUT);
+  unsigned* recs = reinterpret_cast<unsigned*>(smem_raw + L.recs);
+  unsigned* rkeys = KEYS_OUT ? reinterpret_cast<unsigned*>(smem_raw + L.rkeys) : recs;
+  U* sval = reinterpret_cast<U*>(smem_raw + L.vals);
+  int32_t* sidx = reinterpret_cast<int32_t*>(smem_raw + L.idx);
+  unsigned* cnt = reinterpret_cast<unsigned*>(smem_raw + L.cnt);
+  unsigned* off = reinterpret_cast<unsigned*>(smem_raw + L.off);
 
   const long long tile = blockIdx.x;
   const long long N = FIRST ? a.n : (long long)*a.n_valid;
-  const long long K = (long long)blockDim.x * kIPT;
+  const long long K = (long long)T * kIPT;
   const long long tile_base = tile * K;
   if (tile_base >= N) return;
-  const long long wbase = tile_base + (long long)warp * 32 * kIPT;
-  {
-    // the payloads are read after the ranking: start moving them into L2 now
-    const long long cnt = min(K, N - tile_base);
-    if (VB) prefetch_l2(reinterpret_cast<const unsigned char*>(a.vals_in) + tile_base * VB, (size_t)cnt * VB, tid, 32);
-    if (IDX && !FIRST) prefetch_l2(a.idx_in + tile_base, (size_t)cnt * 4, tid, 32);
+  const int cn = (int)min(K, N - tile_base);   // records of this tile
+
+  // ---- payloads (values, carried indices): one bulk copy each for a full,
+  // aligned tile, landing while the keys are ranked; plain loads otherwise
+  constexpr bool PAYLOAD = VB > 0 || IDX_IN;
+  const unsigned char* vsrc = reinterpret_cast<const unsigned char*>(a.vals_in) + tile_base * VB;
+  const int32_t* isrc = IDX_IN ? a.idx_in + tile_base : nullptr;
+  const bool bulk = PAYLOAD && cn == K && (VB == 0 || (reinterpret_cast<uintptr_t>(vsrc) & 15) == 0) &&
+                    (!IDX_IN || (reinterpret_cast<uintptr_t>(isrc) & 15) == 0);
+  if (bulk && tid == 0) {
+    mbar_init(&pay_bar, 1);
+    mbar_arrive_expect_tx(&pay_bar, (unsigned)(K * VB + (IDX_IN ? K * 4 : 0)));
+    if (VB) bulk_copy_g2s(sval, vsrc, (unsigned)(K * VB), &pay_bar);
+    if (IDX_IN) bulk_copy_g2s(sidx, isrc, (unsigned)(K * 4), &pay_bar);
+  }
+  if (PAYLOAD && !bulk)
+    for (int p = tid; p < cn; p += T) {
+      if (VB) sval[p] = __ldg(reinterpret_cast<const U*>(vsrc) + p);
+      if (IDX_IN) sidx[p] = __ldg(isrc + p);
+    }
+
+  // ---- raw keys into the swizzled record array: 16-byte asynchronous
+  // copies for a full, aligned tile (32 KB in flight per CTA), completed
+  // after the digit offsets below
+  const int32_t* ksrc = a.keys_in + tile_base;
+  const bool kasync = cn == K && (reinterpret_cast<uintptr_t>(ksrc) & 15) == 0;
+  if (kasync) {
+    for (int g = tid; g < (int)(K / 4); g += T)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(rkeys + swz(4u * g))),
+                   "l"(ksrc + 4 * g)
+                   : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  } else {
+    for (int p = tid; p < (int)K; p += T) rkeys[swz(p)] = p < cn ? (unsigned)__ldg(ksrc + p) : 0u;
   }
 
-  // ---- this tile's digits; record order = (round, lane) = input order.
-  // A full, aligned tile comes in by one bulk copy into the front of shared
-  // memory (the ranking arrays, zeroed only after the digit-start scan's
-  // barriers): 4-byte loads from every thread cannot keep enough requests in
-  // flight.  Other tiles use plain loads.
-  unsigned packed[kIPT];
-  __shared__ __align__(8) unsigned long long keys_bar;
-  const bool bulk = (N - tile_base) >= K &&
-                    (size_t)K * 4 <= pass_front_bytes(nwarps, ndig, a.K, VB, IDX, KEYS_OUT, STAGE) &&
-                    (reinterpret_cast<uintptr_t>(a.keys_in + tile_base) & 15) == 0;
-  if (bulk) {
-    if (tid == 0) {
-      mbar_init(&keys_bar, 1);
-      mbar_arrive_expect_tx(&keys_bar, (unsigned)(K * 4));
-      bulk_copy_g2s(smem_raw, a.keys_in + tile_base, (unsigned)(K * 4), &keys_bar);
+  // ---- per digit d: global position of the tile's first record of d, less
+  // d's tile-local start.  With E the column prefixes (row `tiles` holds the
+  // totals) and c = E[tile + 1] - E[tile] the tile's own counts:
+  //   off[d] = (sum_{d' < d} total[d'] + E[tile][d]) - sum_{d' < d} c[d']
+  if (tile == 0 && a.seg_out) {   // digit = destination: the digit starts are the segment starts
+    digit_starts(a.totals, ndig, off, wsum);
+    for (long long b = tid; b <= a.m; b += T) a.seg_out[b] = (int32_t)off[b];
+    __syncthreads();
+  }
+  unsigned nvalid_tile;
+  {
+    constexpr int kMaxPer = 1024 / 256;   // digits per thread at most
+    const int per = (ndig + T - 1) / T;
+    const unsigned* e0 = a.counts + tile * ndig;
+    const unsigned* e1 = e0 + ndig;
+    unsigned x[kMaxPer], b0[kMaxPer], loc = 0;
+#pragma unroll
+    for (int k = 0; k < kMaxPer; ++k) {
+      const int d = tid * per + k;
+      x[k] = 0u;
+      b0[k] = 0u;
+      if (k < per && d < ndig) {
+        b0[k] = e0[d];
+        x[k] = a.totals[d] - (e1[d] - b0[k]);
+        loc += x[k];
+      }
     }
-    __syncthreads();   // the barrier is initialised before anyone waits on it
-    const bool ok = mbar_wait(&keys_bar, 0, kWaitNs);
+    unsigned tot;
+    unsigned run = block_excl_scan(loc, wsum, &tot);
+#pragma unroll
+    for (int k = 0; k < kMaxPer; ++k) {
+      const int d = tid * per + k;
+      if (k < per && d < ndig) off[d] = b0[k] + run;
+      run += x[k];
+    }
+    nvalid_tile = *a.n_valid - tot;   // sum of the tile's counts
+    if (nvalid_tile > (unsigned)cn) {   // cannot happen with consistent counts
+      if (tid == 0) set_status(a.status, DET_ERR_INVALID_ARG);
+      nvalid_tile = 0u;
+    }
+  }
+
+  if (kasync) asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+
+  // ---- this thread's records: digit and tile-local index, or the dropped flag
+  unsigned rec[kIPT];
+  load_row(rec, rkeys);
+  {
+    const unsigned m32 = (unsigned)min(a.m, (long long)0x80000000LL);   // keys are int32
+    const bool plain = !FIRST || a.key_offset == 0;
+#pragma unroll
+    for (int j = 0; j < kIPT; ++j) {
+      const unsigned li = (unsigned)(tid * kIPT + j);
+      const unsigned k = rec[j];
+      bool ok = li < (unsigned)cn;
+      unsigned kk = k;
+      if (FIRST) {
+        if (plain) {
+          ok = ok && k < m32;
+        } else {
+          const long long o = (long long)(int32_t)k + a.key_offset;
+          ok = ok && o >= 0 && o < a.m;
+          kk = (unsigned)o;
+        }
+      }
+      const unsigned d = (kk >> a.shift) & mask;
+      rec[j] = ok ? (d << kIdxBits) | li : kDropped | li;
+    }
+  }
+
+  // ---- stable ranking inside the tile
+  if (ndig <= 32) {
+    rank_subpass<kIdxBits, true>(rec, recs, cnt, wsum);
+  } else {
+    rank_subpass<kIdxBits, false>(rec, recs, cnt, wsum);
+    rank_subpass<kIdxBits + 5, true>(rec, recs, cnt, wsum);
+  }
+
+  if (bulk) {
+    const bool ok = mbar_wait(&pay_bar, 0, kWaitNs);
     if (__syncthreads_or(!ok)) {
       // the copy did not complete: record it, give it (bounded) time to land, leave
       if (tid == 0) {
         set_status(a.status, DET_ERR_COPY_TIMEOUT);
-        mbar_wait(&keys_bar, 0, kWaitNs);
+        mbar_wait(&pay_bar, 0, kWaitNs);
       }
       __syncthreads();
       return;
     }
-    const int32_t* sk = reinterpret_cast<const int32_t*>(smem_raw) + warp * 32 * kIPT;
-#pragma unroll
-    for (int r = 0; r < kIPT; ++r) packed[r] = digit_of<FIRST>(a, sk[r * 32 + lane], mask);
-  } else {
-#pragma unroll
-    for (int r = 0; r < kIPT; ++r) packed[r] = record_digit<FIRST, true>(a, wbase + (long long)r * 32 + lane, N, mask);
   }
 
-  // digit starts (from the column totals) plus this tile's column prefixes
-  if (tid == 0) n_digits = 0u;
-  digit_starts(a.totals, ndig, gbase, wsum);
-  if (tile == 0 && a.seg_out)   // digit = destination: the digit starts are the segment starts
-    for (long long b = tid; b <= a.m; b += blockDim.x) a.seg_out[b] = (int32_t)gbase[b];
-  for (int d = tid; d < ndig; d += blockDim.x) gbase[d] += a.counts[tile * ndig + d];
-  for (int d = lane; d < ndig; d += 32) {
-    wcnt[warp * ndig + d] = 0;
-    pmask[warp * ndig + d] = 0u;
-  }
-  __syncwarp();
-
-  // ---- rank inside the warp
-  // The lanes of a round that share a digit ("peers") are found without a
-  // warp vote per digit bit: lanes with lane 0's digit by one ballot, the
-  // others by OR-ing their lane bit into a per-warp mask word of their digit
-  // (OR is order-free, so the mask -- and the rank -- are deterministic).
-  unsigned* pm = pmask + warp * ndig;
-  unsigned short* wc = wcnt + warp * ndig;
-#pragma unroll
-  for (int r = 0; r < kIPT; ++r) {
-    const unsigned d = packed[r];
-    const bool valid = d != 0xffffffffu;
-    const unsigned d0 = __shfl_sync(0xffffffffu, d, 0);
-    const bool in0 = valid && d == d0;
-    const unsigned same0 = __ballot_sync(0xffffffffu, in0);
-    if (valid && !in0) atomicOr(pm + d, 1u << lane);
-    __syncwarp();
-    const unsigned peers = in0 ? same0 : (valid ? pm[d] : 0u);
-    const unsigned base = valid ? wc[d] : 0u;
-    __syncwarp();
-    if (valid && lane == __ffs(peers) - 1) {
-      wc[d] = (unsigned short)(base + __popc(peers));
-      if (!in0) pm[d] = 0u;
-    }
-    __syncwarp();
-    packed[r] = valid ? ((d << 16) | (base + __popc(peers & ((1u << lane) - 1u)))) : 0xffffffffu;
-  }
-  __syncthreads();
-
-  if (!STAGE) {
-    // ---- direct scatter (payloads too large to stage): warp prefixes, then
-    // each record goes straight to its global position
-    for (int d = tid; d < ndig; d += blockDim.x) {
-      unsigned run = 0;
-      for (int w = 0; w < nwarps; ++w) {
-        const unsigned c = wcnt[w * ndig + d];
-        wcnt[w * ndig + d] = (unsigned short)run;
-        run += c;
-      }
-    }
-    __syncthreads();
-    const U* __restrict__ vin = reinterpret_cast<const U*>(a.vals_in);
-    U* __restrict__ vout = reinterpret_cast<U*>(a.vals_out);
-    const int32_t* __restrict__ iin = a.idx_in;
-    int32_t* __restrict__ iout = a.idx_out;
-    const int32_t* __restrict__ kin = a.keys_in;
-    int32_t* __restrict__ kout = a.keys_out;
-    const unsigned short* __restrict__ wc_tile = wcnt + warp * ndig;
-    constexpr int B = 4;
-#pragma unroll
-    for (int r0 = 0; r0 < kIPT; r0 += B) {
-      U vv[B];
-      int32_t ii[B], kk[B];
-#pragma unroll
-      for (int e = 0; e < B; ++e) {
-        const long long i = wbase + (long long)(r0 + e) * 32 + lane;
-        const bool ok = packed[r0 + e] != 0xffffffffu;
-        if (VB) vv[e] = ok ? __ldg(vin + i) : U(0);
-        if (IDX) ii[e] = ok ? (FIRST ? (int32_t)i : __ldg(iin + i)) : 0;
-        if (KEYS_OUT) kk[e] = ok ? (FIRST ? (int32_t)((long long)__ldg(kin + i) + a.key_offset) : __ldg(kin + i)) : 0;
-      }
-#pragma unroll
-      for (int e = 0; e < B; ++e) {
-        const unsigned pk = packed[r0 + e];
-        if (pk == 0xffffffffu) continue;
-        const unsigned d = pk >> 16;
-        const long long pos = (long long)gbase[d] + wc_tile[d] + (pk & 0xffffu);
-        if (pos < 0 || pos >= a.n) {
-          set_status(a.status, DET_ERR_INVALID_ARG);
-          continue;
-        }
-        if (VB) vout[pos] = vv[e];
-        if (IDX) iout[pos] = ii[e];
-        if (KEYS_OUT) kout[pos] = kk[e];
-      }
-    }
-    return;
-  }
-
-  // ---- per digit: exclusive prefix over the warps of this tile, and the
-  // tile's digit counts
-  unsigned int* lstart = gbase + (ndig + 1);   // [ndig + 1] tile-local digit starts
-  {
-    unsigned nz = 0;
-    for (int d = tid; d < ndig; d += blockDim.x) {
-      unsigned run = 0;
-      for (int w = 0; w < nwarps; ++w) {
-        const unsigned c = wcnt[w * ndig + d];
-        wcnt[w * ndig + d] = (unsigned short)run;
-        run += c;
-      }
-      lstart[d] = run;   // count for now; turned into starts below
-      nz += run != 0;
-    }
-    if (nz) atomicAdd(&n_digits, nz);
-  }
-  __syncthreads();
-  {
-    // exclusive scan of the tile's digit counts (reuses the digit-start scan)
-    unsigned int* tmp = gbase + 2 * (ndig + 1);   // [ndig + 1]
-    digit_starts(lstart, ndig, tmp, wsum);
-    for (int d = tid; d <= ndig; d += blockDim.x) lstart[d] = tmp[d];
-  }
-  __syncthreads();
-  // tile-local sorted position of each record (digit-major, stable)
-#pragma unroll
-  for (int r = 0; r < kIPT; ++r) {
-    const unsigned pk = packed[r];
-    if (pk == 0xffffffffu) continue;
-    const unsigned d = pk >> 16;
-    packed[r] = (d << 16) | (lstart[d] + wcnt[warp * ndig + d] + (pk & 0xffffu));
-  }
-  if (a.rank_out) {
-    // only each record's sorted position is wanted: write it in input order
-    // (coalesced) and move nothing
-#pragma unroll
-    for (int r = 0; r < kIPT; ++r) {
-      const unsigned pk = packed[r];
-      if (pk == 0xffffffffu) continue;
-      const unsigned d = pk >> 16;
-      a.rank_out[wbase + (long long)r * 32 + lane] = (int32_t)(gbase[d] - lstart[d] + (pk & 0xffffu));
-    }
-    return;
-  }
-  __syncthreads();   // the peer-mask and counter words are free from here on
-
-  // ---- one-pass sorts of full, aligned tiles whose digit runs are long (16
-  // records or more on average, so that a warp's stores mostly fall in one
-  // run): the tile's values come in by one bulk copy (input order) into the
-  // freed front of shared memory, and each thread stores its records' values
-  // straight to their global places.  Short runs go through the staging below.
-  const size_t front_bytes = pass_front_bytes(nwarps, ndig, a.K, VB, IDX, KEYS_OUT, STAGE);
-  if (VB > 0 && !KEYS_OUT && (!IDX || FIRST) && (N - tile_base) >= K && (size_t)K * VB <= front_bytes &&
-      lstart[ndig] >= 16u * n_digits &&
-      (reinterpret_cast<uintptr_t>(reinterpret_cast<const unsigned char*>(a.vals_in) + tile_base * VB) & 15) == 0) {
-    __shared__ __align__(8) unsigned long long vals_bar;
-    if (tid == 0) {
-      // the front was last written by ordinary stores: order them before the copy engine's writes
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_init(&vals_bar, 1);
-      mbar_arrive_expect_tx(&vals_bar, (unsigned)(K * VB));
-      bulk_copy_g2s(smem_raw, reinterpret_cast<const unsigned char*>(a.vals_in) + tile_base * VB, (unsigned)(K * VB),
-                    &vals_bar);
-    }
-    // global position of each record: local position + (global - local digit start)
-#pragma unroll
-    for (int r = 0; r < kIPT; ++r) {
-      const unsigned pk = packed[r];
-      if (pk == 0xffffffffu) continue;
-      const unsigned d = pk >> 16;
-      packed[r] = gbase[d] - lstart[d] + (pk & 0xffffu);
-    }
-    __syncthreads();   // the barrier is initialised before anyone waits on it
-    const bool ok = mbar_wait(&vals_bar, 0, kWaitNs);
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) {
-        set_status(a.status, DET_ERR_COPY_TIMEOUT);
-        mbar_wait(&vals_bar, 0, kWaitNs);
-      }
-      __syncthreads();
-      return;
-    }
-    const U* sv = reinterpret_cast<const U*>(smem_raw) + warp * 32 * kIPT;
-    U* __restrict__ vout = reinterpret_cast<U*>(a.vals_out);
-#pragma unroll
-    for (int r = 0; r < kIPT; ++r) {
-      const unsigned pos = packed[r];
-      if (pos == 0xffffffffu) continue;
-      if ((long long)pos >= a.n) {   // cannot happen for a correct ranking; never write out of bounds
-        set_status(a.status, DET_ERR_INVALID_ARG);
-        continue;
-      }
-      vout[pos] = sv[r * 32 + lane];
-      if (IDX) a.idx_out[pos] = (int32_t)(wbase + (long long)r * 32 + lane);
-    }
-    return;
-  }
-
-  // ---- stage the records in shared memory in tile-sorted order, then write
-  // each digit's run to its global place with consecutive threads on
-  // consecutive positions (coalesced runs instead of one sector per record)
-  const long long nvalid_tile = lstart[ndig];
-  unsigned char* stage = smem_raw;   // overlaps pmask / wcnt
-  U* s_val = reinterpret_cast<U*>(stage);
-  int32_t* s_idx = reinterpret_cast<int32_t*>(stage + (size_t)VB * a.K);
-  int32_t* s_key = reinterpret_cast<int32_t*>(stage + (size_t)(VB + (IDX ? 4 : 0)) * a.K);
-  unsigned short* s_dig =
-      reinterpret_cast<unsigned short*>(stage + (size_t)(VB + (IDX ? 4 : 0) + (KEYS_OUT ? 4 : 0)) * a.K);
-  const U* __restrict__ vin = reinterpret_cast<const U*>(a.vals_in);
+  // ---- write out in sorted order: runs of one digit are consecutive
+  // positions, so consecutive threads store to consecutive addresses
   U* __restrict__ vout = reinterpret_cast<U*>(a.vals_out);
-  const int32_t* __restrict__ iin = a.idx_in;
-  int32_t* __restrict__ iout = a.idx_out;
-  const int32_t* __restrict__ kin = a.keys_in;
-  int32_t* __restrict__ kout = a.keys_out;
-  // payloads go from global memory (L2, prefetched above) straight to their
-  // sorted slot by asynchronous copies: no registers, one round trip
-#pragma unroll
-  for (int r = 0; r < kIPT; ++r) {
-    const unsigned pk = packed[r];
-    if (pk == 0xffffffffu) continue;
-    const long long i = wbase + (long long)r * 32 + lane;
-    const unsigned lp = pk & 0xffffu;
-    if (VB) cp_async_small<VB>(s_val + lp, vin + i);
-    if (IDX) {
-      if (FIRST)
-        s_idx[lp] = (int32_t)i;
-      else
-        cp_async_small<4>(s_idx + lp, iin + i);
-    }
-    if (KEYS_OUT) cp_async_small<4>(s_key + lp, kin + i);   // raw key; the offset is added on the way out
-    s_dig[lp] = (unsigned short)(pk >> 16);
-  }
-  // global position = local position + (global digit start - local digit start)
-  for (int d = tid; d < ndig; d += blockDim.x) gbase[d] -= lstart[d];
-  cp_async_commit_wait_all();
-  __syncthreads();
+  const unsigned n32 = (unsigned)a.n;   // sort sizes are below 2^31
+  bool bad = false;
 #pragma unroll 4
-  for (long long i = tid; i < nvalid_tile; i += blockDim.x) {
-    const unsigned d = s_dig[i];
-    const long long pos = (long long)gbase[d] + i;
-    if (pos < 0 || pos >= a.n) {   // cannot happen for a correct ranking; never write out of bounds
-      set_status(a.status, DET_ERR_INVALID_ARG);
-      continue;
+  for (unsigned p = tid; p < nvalid_tile; p += T) {
+    const unsigned r = recs[swz(p)];
+    const unsigned d = r >> kIdxBits, li = r & ((1u << kIdxBits) - 1u);
+    const unsigned pos = off[d & mask] + p;
+    // cannot fail for a correct ranking; never write out of bounds
+    const bool ok = d < (unsigned)ndig && pos < n32;
+    bad |= !ok;
+    if (ok) {
+      if (RANK) a.rank_out[tile_base + li] = (int32_t)pos;
+      if (VB) vout[pos] = sval[li];
+      if (IDX) a.idx_out[pos] = IDX_IN ? sidx[li] : (int32_t)(tile_base + li);
+      if (KEYS_OUT) {
+        const int32_t k = (int32_t)rkeys[swz(li)];
+        a.keys_out[pos] = FIRST ? (int32_t)((long long)k + a.key_offset) : k;
+      }
     }
-    if (VB) vout[pos] = s_val[i];
-    if (IDX) iout[pos] = s_idx[i];
-    if (KEYS_OUT) kout[pos] = FIRST ? (int32_t)((long long)s_key[i] + a.key_offset) : s_key[i];
   }
+  if (bad) set_status(a.status, DET_ERR_INVALID_ARG);
 }
 
 // seg[b] = first sorted position with key >= b, for b = 0..m (keys sorted).
+// Thread t covers positions [4t, 4t + 4) -- four keys by one 16-byte load --
+// and, for the thread that reaches it, position N (the valid count), where
+// every remaining bin starts.
 __global__ void sort_bounds_kernel(const int32_t* __restrict__ keys, const unsigned int* __restrict__ n_valid,
                                    long long m, int32_t* __restrict__ seg, long long n) {
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long N = *n_valid;
-  if (i > N || i > n) return;
-  const long long prev = (i == 0) ? -1 : max(-1LL, min((long long)keys[i - 1], m));
-  const long long cur = (i == N) ? m : max(-1LL, min((long long)keys[i], m));
-  for (long long b = prev + 1; b <= cur; ++b) seg[b] = (int32_t)i;
+  const long long i0 = 4 * ((long long)blockIdx.x * blockDim.x + threadIdx.x);
+  const long long N = min((long long)*n_valid, n);
+  if (i0 > N) return;
+  auto clampk = [&](int32_t k) { return max(-1LL, min((long long)k, m)); };
+  long long k[5];   // k[0]: the key before i0; k[1 + e]: the key at i0 + e (m from N on)
+  k[0] = i0 == 0 ? -1 : clampk(__ldg(keys + i0 - 1));
+  if (i0 + 4 <= N && (reinterpret_cast<uintptr_t>(keys + i0) & 15) == 0) {
+    const int4 q = __ldg(reinterpret_cast<const int4*>(keys + i0));
+    k[1] = clampk(q.x);
+    k[2] = clampk(q.y);
+    k[3] = clampk(q.z);
+    k[4] = clampk(q.w);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) k[1 + e] = i0 + e < N ? clampk(__ldg(keys + i0 + e)) : m;
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if (i0 + e > N) break;
+    for (long long b = k[e] + 1; b <= k[e + 1]; ++b) seg[b] = (int32_t)(i0 + e);
+  }
 }
-
 
 // ---------------------------------------------------------------------------
 // PT over p[0..len) by one warp: rounds of 256 (8 per lane, in-register tree,
@@ -612,76 +658,149 @@ struct LongSeg {
   long long nblk;
 };
 
+// One rank-aligned block of a long bin: its leaves are vals[lo, lo + len).
+struct BlockDesc {
+  long long lo;
+  unsigned int len;
+  unsigned int sidx;   // the bin's entry in the long-segment list
+};
+
+constexpr int kMediumGroup = 1024;   // groups up to this size are reduced by one warp
+
+// Leaves [0, W) of a short group by one thread: the group's len <= W values
+// (negated for NEG) padded with absent terms, then the in-register tree --
+// PT padded to W, which is PT of the group.
+template <typename T, bool NEG, int W>
+__device__ __forceinline__ T thread_group_pt(const T* __restrict__ p, long long len) {
+  T v[W];
+#pragma unroll
+  for (int e = 0; e < W; ++e) {
+    if (e < len) {
+      const T x = __ldg(p + e);
+      v[e] = NEG ? -x : x;
+    } else {
+      v[e] = absent<T>();
+    }
+  }
+  return thread_pt(v);
+}
+
+// One thread per bin b: out[b] = out[b] + PT(group b).
+//   groups of at most 32 records: the thread's own in-register tree
+//   up to kMediumGroup records: the whole warp, one such group at a time
+//   longer groups: cut into rank-aligned 4096-blocks (subtrees of the
+//     group's tree) for the block kernel; the warp writes their list
 // NEG: the tree is over the negated values (scatter-sub).  The leaves are
 // negated, not the result: an exact zero from cancellation is +0.0 either
 // way, so -PT(v) and PT(-v) can differ in the sign of a zero.
 template <typename T, bool NEG>
 __global__ void __launch_bounds__(256)
 segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg, long long m, T* __restrict__ out,
-                    long long* __restrict__ blocks, LongSeg* __restrict__ lsegs, unsigned int* __restrict__ ldone,
+                    BlockDesc* __restrict__ blocks, LongSeg* __restrict__ lsegs, unsigned int* __restrict__ ldone,
                     unsigned int* __restrict__ nblocks, unsigned int* __restrict__ nlsegs,
                     const unsigned int* __restrict__ n_valid, long long max_blocks, long long max_lsegs,
                     unsigned int* __restrict__ status, long long ostride) {
-  const long long b = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int lane = threadIdx.x & 31;
-  if (b >= m) return;
   const long long N = *n_valid;
-  const long long hi = min((long long)seg[b + 1], N), lo = max(0LL, min((long long)seg[b], hi));
-  const long long len = hi - lo;
-  if (len <= 0) return;
-  if (len <= kSegBlock) {
-    const T t = warp_pt_range<T, false, NEG>(vals + lo, len);
-    if (lane == 0) out[b * ostride] = out[b * ostride] + t;
-    return;
+  long long lo = 0, len = 0;
+  if (b < m) {
+    const long long hi = min((long long)seg[b + 1], N);
+    lo = max(0LL, min((long long)seg[b], hi));
+    len = hi - lo;
   }
-  const long long nblk = (len + kSegBlock - 1) / kSegBlock;
-  long long base = 0, sidx = 0;
-  if (lane == 0) {
-    base = atomicAdd(nblocks, (unsigned)nblk);
-    sidx = atomicAdd(nlsegs, 1u);
-    if (sidx < max_lsegs && base + nblk <= max_blocks) {
+  if (len > 0 && len <= 32) {
+    T t;
+    if (len <= 4)
+      t = thread_group_pt<T, NEG, 4>(vals + lo, len);
+    else if (len <= 8)
+      t = thread_group_pt<T, NEG, 8>(vals + lo, len);
+    else if (len <= 16)
+      t = thread_group_pt<T, NEG, 16>(vals + lo, len);
+    else
+      t = thread_group_pt<T, NEG, 32>(vals + lo, len);
+    out[b * ostride] = out[b * ostride] + t;
+  }
+  // the warp's medium groups, one at a time
+  unsigned med = __ballot_sync(0xffffffffu, len > 32 && len <= kMediumGroup);
+  while (med) {
+    const int src = __ffs(med) - 1;
+    med &= med - 1;
+    const long long mlo = __shfl_sync(0xffffffffu, lo, src), mlen = __shfl_sync(0xffffffffu, len, src);
+    const T t = warp_pt_range<T, false, NEG>(vals + mlo, mlen);
+    if (lane == src) out[b * ostride] = out[b * ostride] + t;
+  }
+  // long groups: their blocks are reserved (the reservation order does not
+  // matter: a group's tree reads only its own nodes), then the warp writes
+  // the block list of its long groups one at a time
+  const bool is_long = len > kMediumGroup;
+  const long long nblk = is_long ? (len + kSegBlock - 1) / kSegBlock : 0;
+  // one reservation per warp: exclusive prefixes of the block counts and of
+  // the long groups over the lanes, lane 31 adding the warp's totals
+  long long pre = nblk;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const long long o = __shfl_up_sync(0xffffffffu, pre, d);
+    if (lane >= d) pre += o;
+  }
+  const unsigned longs = __ballot_sync(0xffffffffu, is_long);
+  long long wbase = 0, wsidx = 0;
+  if (lane == 31 && longs) {
+    wbase = atomicAdd(nblocks, (unsigned)pre);
+    wsidx = atomicAdd(nlsegs, (unsigned)__popc(longs));
+  }
+  wbase = __shfl_sync(0xffffffffu, wbase, 31);
+  wsidx = __shfl_sync(0xffffffffu, wsidx, 31);
+  const long long base = wbase + pre - nblk;
+  const long long sidx = wsidx + __popc(longs & ((1u << lane) - 1u));
+  bool reg = false;
+  if (is_long) {
+    reg = sidx < max_lsegs && base + nblk <= max_blocks;
+    if (reg) {
       lsegs[sidx] = LongSeg{b, base, nblk};
       ldone[sidx] = 0u;
     } else {
       set_status(status, DET_ERR_INVALID_ARG);
     }
   }
-  base = __shfl_sync(0xffffffffu, base, 0);
-  sidx = __shfl_sync(0xffffffffu, sidx, 0);
-  if (sidx >= max_lsegs || base + nblk > max_blocks) return;
-  for (long long k = lane; k < nblk; k += 32) blocks[base + k] = (sidx << 24) | k;
+  unsigned lng = __ballot_sync(0xffffffffu, reg);
+  while (lng) {
+    const int src = __ffs(lng) - 1;
+    lng &= lng - 1;
+    const long long glo = __shfl_sync(0xffffffffu, lo, src), glen = __shfl_sync(0xffffffffu, len, src);
+    const long long gbase = __shfl_sync(0xffffffffu, base, src), gn = __shfl_sync(0xffffffffu, nblk, src);
+    const unsigned gs = (unsigned)__shfl_sync(0xffffffffu, sidx, src);
+    for (long long k = lane; k < gn; k += 32)
+      blocks[gbase + k] =
+          BlockDesc{glo + k * kSegBlock, (unsigned)min((long long)kSegBlock, glen - k * kSegBlock), gs};
+  }
 }
 
-// One CTA of 256 threads per rank-aligned 2048-record block of a long bin.
-// All leaves are read in one coalesced round into shared memory; thread t
-// then takes leaves [8t, 8t+8) (a level-3 node), the warp's butterfly gives
-// the level-8 node and the tree over the 8 warps the level-11 node -- the
-// same node as any other aligned decomposition of the block.  The CTA that
-// completes a bin's last block (a per-bin counter) forms the PT over the
-// bin's block nodes and adds it to out[bin]: who does it varies, the tree
-// does not.
+// One CTA of 256 threads per rank-aligned 4096-record block of a long bin.
+// All leaves are read in one coalesced round (16 loads per thread in
+// flight) into shared memory; thread t then takes leaves [8t, 8t+8) of each
+// 2048-record half (a level-3 node), the warp's butterfly gives the level-8
+// node, the tree over the 8 warps the level-11 node and the two halves the
+// level-12 node -- the same node as any other aligned decomposition of the
+// block.  The CTA that completes a bin's last block (a per-bin counter)
+// forms the PT over the bin's block nodes and adds it to out[bin]: who does
+// it varies, the tree does not.
 template <typename T, bool NEG>
 __global__ void __launch_bounds__(256)
-segtree_blocks_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg, const long long* __restrict__ blocks,
+segtree_blocks_kernel(const T* __restrict__ vals, const BlockDesc* __restrict__ blocks,
                       const unsigned int* __restrict__ nblocks, const LongSeg* __restrict__ lsegs,
-                      unsigned int* __restrict__ ldone, T* nodes, T* __restrict__ out,
-                      const unsigned int* __restrict__ n_valid, long long max_blocks, long long max_lsegs,
-                      long long ostride) {
-  static_assert(kSegBlock == 256 * 8, "one CTA of 256 threads x 8 leaves per block");
+                      unsigned int* __restrict__ ldone, T* nodes, T* __restrict__ out, long long max_blocks,
+                      long long max_lsegs, long long ostride) {
+  static_assert(kSegBlock == 2 * 256 * 8, "one CTA of 256 threads x 8 leaves per half block");
   __shared__ __align__(16) T buf[kSegBlock];
-  __shared__ T wnode[8];
+  __shared__ T wnode[2][8];
   __shared__ int last;
   const long long q = blockIdx.x;
   if (q >= (long long)*nblocks || q >= max_blocks) return;
   const int tid = threadIdx.x;
-  const long long e = blocks[q];
-  const long long sidx = e >> 24, k = e & ((1 << 24) - 1);
-  if (sidx >= max_lsegs) return;
-  const LongSeg L = lsegs[sidx];
-  const long long N = *n_valid;
-  const long long hi = min((long long)seg[L.bin + 1], N);
-  const long long lo = max(0LL, min((long long)seg[L.bin] + k * kSegBlock, hi));
-  const long long len = min((long long)kSegBlock, hi - lo);
+  const BlockDesc B = blocks[q];
+  if (B.sidx >= max_lsegs) return;
+  const long long lo = B.lo, len = min((long long)kSegBlock, (long long)B.len);
 #pragma unroll
   for (int i = 0; i < kSegBlock / 256; ++i) {
     const int j = i * 256 + tid;
@@ -689,24 +808,33 @@ segtree_blocks_kernel(const T* __restrict__ vals, const int32_t* __restrict__ se
   }
   __syncthreads();
   constexpr int NQ = 8 * (int)sizeof(T) / 16;
-  float4 q4[NQ];
 #pragma unroll
-  for (int i = 0; i < NQ; ++i) q4[i] = reinterpret_cast<const float4*>(buf + tid * 8)[i];
-  T v[8];
-  memcpy(v, q4, sizeof(v));
-  const T node = warp_pt(thread_pt(v));
-  if ((tid & 31) == 0) wnode[tid >> 5] = node;
+  for (int h = 0; h < 2; ++h) {
+    float4 q4[NQ];
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) q4[i] = reinterpret_cast<const float4*>(buf + h * (kSegBlock / 2) + tid * 8)[i];
+    T v[8];
+    memcpy(v, q4, sizeof(v));
+    const T node = warp_pt(thread_pt(v));
+    if ((tid & 31) == 0) wnode[h][tid >> 5] = node;
+  }
   __syncthreads();
   if (tid == 0) {
-    const T a01 = wnode[0] + wnode[1], a23 = wnode[2] + wnode[3];
-    const T a45 = wnode[4] + wnode[5], a67 = wnode[6] + wnode[7];
-    nodes[q] = (a01 + a23) + (a45 + a67);
+    T half[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const T a01 = wnode[h][0] + wnode[h][1], a23 = wnode[h][2] + wnode[h][3];
+      const T a45 = wnode[h][4] + wnode[h][5], a67 = wnode[h][6] + wnode[h][7];
+      half[h] = (a01 + a23) + (a45 + a67);
+    }
+    nodes[q] = half[0] + half[1];
     __threadfence();
-    last = atomicAdd(&ldone[sidx], 1u) == (unsigned)(L.nblk - 1);
+    last = atomicAdd(&ldone[B.sidx], 1u) == (unsigned)(lsegs[B.sidx].nblk - 1);
   }
   __syncthreads();
   if (last && tid < 32) {
     __threadfence();
+    const LongSeg L = lsegs[B.sidx];
     const T t = warp_pt_range<T, true>(nodes + L.base, L.nblk);   // nodes already hold the negated leaves
     if (tid == 0) out[L.bin * ostride] = out[L.bin * ostride] + t;
   }
@@ -715,6 +843,17 @@ segtree_blocks_kernel(const T* __restrict__ vals, const int32_t* __restrict__ se
 }  // namespace
 
 // ---------------------------------------------------------------------------
+
+// Warps of the passes that stay resident on one SM with CTAs of T threads:
+// 228 KB of shared memory per SM, 1 KB of it reserved per CTA; registers
+// (at most 64 per thread) allow two CTAs of 512 threads or four of 256.
+static int resident_pass_warps(const SortPlan& p, int T) {
+  size_t worst = 0;
+  for (int pass = 0; pass < p.passes; ++pass)
+    worst = std::max(worst, pass_smem(T, 1 << p.digit_bits, p.value_bytes, p.need_idx && pass > 0, p.passes > 1).total);
+  const long long ctas = std::min<long long>(233472 / (long long)(worst + 1024 + 256), T == 512 ? 2 : 4);
+  return (int)ctas * (T / 32);
+}
 
 SortPlan make_sort_plan(long long n, long long m, int value_bytes, bool need_idx, int block_threads) {
   SortPlan p;
@@ -726,13 +865,19 @@ SortPlan make_sort_plan(long long n, long long m, int value_bytes, bool need_idx
   while ((1LL << B) < m) ++B;
   p.passes = B <= 10 ? 1 : (B + 9) / 10;
   p.digit_bits = B == 0 ? 1 : (B + p.passes - 1) / p.passes;
-  // The sort's tile is threads x kIPT records.  block_threads = 128 gives
-  // 4,096-record tiles; every other choice the 8,192-record tiles of 256
-  // threads (the ranking's per-warp digit arrays make larger CTAs pointless),
-  // except that by default sorts of at most 2^22 records take the smaller
-  // tiles, so that they still spread over every SM.  Tiling never changes
-  // the bits: the sort is stable.
-  p.threads = (block_threads == 128 || (block_threads == 0 && n <= (1LL << 22))) ? 128 : 256;
+  // The sort's tile is threads x kIPT records: 4,096 (CTAs of 256 threads)
+  // for block_threads = 128, 8,192 (512 threads) for 256, 512 or 1024.  By
+  // default sorts of at most 2^22 records take the smaller tiles, so that
+  // they still spread over every SM; larger ones take whichever size keeps
+  // more warps resident under the passes' shared memory.  Tiling never
+  // changes the bits: the sort is stable.
+  if (block_threads == 128 || block_threads == 256 || block_threads == 512 || block_threads == 1024) {
+    p.threads = block_threads == 128 ? 256 : 512;
+  } else if (n <= (1LL << 22)) {
+    p.threads = 256;
+  } else {
+    p.threads = resident_pass_warps(p, 512) >= resident_pass_warps(p, 256) ? 512 : 256;
+  }
   p.ipt = kIPT;
   const long long K = (long long)p.threads * kIPT;
   p.tiles = (n + K - 1) / K;
@@ -759,12 +904,13 @@ SortPlan make_sort_plan(long long n, long long m, int value_bytes, bool need_idx
   }
   p.seg = off;
   off = align_up(off + (size_t)(m + 1) * 4, 256);
-  // blocks of long bins: ceil(len / 2048) <= len / 2048 + 1 each, and at most
-  // min(m, n / 2048) bins are long (each holds more than 2048 records)
-  p.max_blocks = n / kSegBlock + std::min(m, n / kSegBlock) + 2;
-  p.max_lsegs = n / kSegBlock + 2;
+  // blocks of long bins: ceil(len / B) <= len / B + 1 each (B = kSegBlock), and
+  // at most min(m, n / kMediumGroup) bins are long (each holds more than
+  // kMediumGroup records)
+  p.max_blocks = n / kSegBlock + std::min(m, n / kMediumGroup) + 2;
+  p.max_lsegs = std::min(m, n / kMediumGroup) + 2;
   p.blocks = off;
-  off = align_up(off + (size_t)p.max_blocks * 8, 256);
+  off = align_up(off + (size_t)p.max_blocks * sizeof(BlockDesc), 256);
   p.lsegs = off;
   off = align_up(off + (size_t)p.max_lsegs * sizeof(LongSeg), 256);
   p.ldone = off;
@@ -779,14 +925,10 @@ template <int VB>
 static cudaError_t launch_pass(const PassArgs& a, bool first, bool idx, bool keys_out, int threads, long long tiles,
                                cudaStream_t s) {
   const int ndig = 1 << a.D;
-  const int max_smem = device_max_smem_optin();
-  const size_t tail = (size_t)3 * (ndig + 1) * 4;
-  const bool stage = pass_front_bytes(threads / 32, ndig, a.K, VB, idx, keys_out, true) + tail <= (size_t)max_smem;
-  const size_t smem = pass_front_bytes(threads / 32, ndig, a.K, VB, idx, keys_out, stage) + tail;
+  const size_t smem = pass_smem(threads, ndig, VB, idx && !first, keys_out).total;
   void (*k)(PassArgs) = nullptr;
-#define DET_PICK(F, I, KO)                                                            \
-  if (first == F && idx == I && keys_out == KO)                                       \
-    k = stage ? sort_pass_kernel<VB, F, I, KO, true> : sort_pass_kernel<VB, F, I, KO, false>;
+#define DET_PICK(F, I, KO) \
+  if (first == F && idx == I && keys_out == KO) k = sort_pass_kernel<VB, F, I, KO>;
   DET_PICK(true, true, true) DET_PICK(true, true, false) DET_PICK(true, false, true) DET_PICK(true, false, false)
   DET_PICK(false, true, true) DET_PICK(false, true, false) DET_PICK(false, false, true) DET_PICK(false, false, false)
 #undef DET_PICK
@@ -835,13 +977,13 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
     a.n_valid = &h->n_valid;
     a.seg_out = p.passes == 1 ? seg : nullptr;
     a.rank_out = p.passes == 1 ? rank_out : nullptr;
-    const size_t csmem = (size_t)ndig * 4;
+    const size_t csmem = align_up((size_t)(ndig + 1) * 4, 16) + (size_t)p.threads * kIPT * 4;
     const long long K = (long long)p.threads * kIPT;
+    void (*ck)(PassArgs, long long) = first ? sort_count_kernel<true> : sort_count_kernel<false>;
+    const cudaError_t ce = ensure_dyn_smem((const void*)ck, csmem);
+    if (ce != cudaSuccess) return cuda_fail(ce, "sort: digit counts");
     launch_begin("det_sort_count", s);
-    if (first)
-      sort_count_kernel<true><<<(unsigned)p.tiles, 256, csmem, s>>>(a, K);
-    else
-      sort_count_kernel<false><<<(unsigned)p.tiles, 256, csmem, s>>>(a, K);
+    ck<<<(unsigned)p.tiles, 256, csmem, s>>>(a, K);
     launch_end(s);
     launch_begin("det_sort_colscan", s);
     sort_colscan_kernel<<<(unsigned)((ndig + kColDigits - 1) / kColDigits), 1024, 0, s>>>(a, first ? 1 : 0);
@@ -860,7 +1002,7 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
   }
   if (p.passes > 1) {   // one-pass sorts got their segment starts from the pass
     launch_begin("det_sort_bounds", s);
-    sort_bounds_kernel<<<(unsigned)((p.n + 1 + 255) / 256), 256, 0, s>>>(
+    sort_bounds_kernel<<<(unsigned)((p.n + 1 + 1023) / 1024), 256, 0, s>>>(
         reinterpret_cast<const int32_t*>(w + p.keys[*final_buf]), &h->n_valid, p.m, seg, p.n);
     launch_end(s);
   }
@@ -874,7 +1016,7 @@ int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T*
   char* w = reinterpret_cast<char*>(ws);
   SortHdr* h = reinterpret_cast<SortHdr*>(ws);
   const int32_t* seg = reinterpret_cast<const int32_t*>(w + p.seg);
-  long long* blocks = reinterpret_cast<long long*>(w + p.blocks);
+  BlockDesc* blocks = reinterpret_cast<BlockDesc*>(w + p.blocks);
   LongSeg* lsegs = reinterpret_cast<LongSeg*>(w + p.lsegs);
   T* nodes = reinterpret_cast<T*>(w + p.nodes);
   unsigned int* ldone = reinterpret_cast<unsigned int*>(w + p.ldone);
@@ -882,7 +1024,7 @@ int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T*
     return DET_ERR_CUDA;
   launch_begin("det_segtree_bins", s);
   auto* kb = negate ? segtree_bins_kernel<T, true> : segtree_bins_kernel<T, false>;
-  kb<<<(unsigned)((p.m * 32 + 255) / 256), 256, 0, s>>>(sorted_vals, seg, p.m, out, blocks, lsegs, ldone,
+  kb<<<(unsigned)((p.m + 255) / 256), 256, 0, s>>>(sorted_vals, seg, p.m, out, blocks, lsegs, ldone,
                                                          &h->long_blocks, &h->long_segs, &h->n_valid, p.max_blocks,
                                                          p.max_lsegs, &h->status, ostride);
   launch_end(s);
@@ -890,8 +1032,8 @@ int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T*
   if (rc != DET_OK) return rc;
   launch_begin("det_segtree_blocks", s);
   auto* kk = negate ? segtree_blocks_kernel<T, true> : segtree_blocks_kernel<T, false>;
-  kk<<<(unsigned)p.max_blocks, 256, 0, s>>>(sorted_vals, seg, blocks, &h->long_blocks, lsegs, ldone, nodes, out,
-                                            &h->n_valid, p.max_blocks, p.max_lsegs, ostride);
+  kk<<<(unsigned)p.max_blocks, 256, 0, s>>>(sorted_vals, blocks, &h->long_blocks, lsegs, ldone, nodes, out,
+                                            p.max_blocks, p.max_lsegs, ostride);
   launch_end(s);
   return check_launch("segmented tree: blocks");
 }

@@ -40,7 +40,7 @@ struct SortHdr {
   unsigned int long_segs;
 };
 
-constexpr int kSegBlock = 2048;   // rank-aligned block of the segmented tree
+constexpr int kSegBlock = 4096;   // rank-aligned block of the segmented tree
 
 SortPlan make_sort_plan(long long n, long long m, int value_bytes, bool need_idx, int block_threads);
 
