@@ -150,10 +150,19 @@ __global__ void __launch_bounds__(1024) sort_colscan_kernel(PassArgs a, int coun
   const long long T = a.tiles;
   const long long TG = (T + kColGroups - 1) / kColGroups;
   const long long t0 = g * TG, t1 = min(T, t0 + TG);
-  // the tiles of a group are read eight at a time (independent loads in flight)
-  constexpr int kU = 8;
+  // a group of at most kR tiles is read once, all loads in flight, and kept
+  // in registers for the rewrite; longer groups are read eight at a time,
+  // twice
+  constexpr int kR = 16, kU = 8;
+  const bool regs = TG <= kR;
+  unsigned r[kR];
   unsigned sum = 0;
-  if (d < ndig)
+  if (d < ndig && regs) {
+#pragma unroll
+    for (int k = 0; k < kR; ++k) r[k] = t0 + k < t1 ? a.counts[(t0 + k) * ndig + d] : 0u;
+#pragma unroll
+    for (int k = 0; k < kR; ++k) sum += r[k];
+  } else if (d < ndig)
     for (long long t = t0; t < t1; t += kU) {
       unsigned v[kU];
 #pragma unroll
@@ -194,7 +203,13 @@ __global__ void __launch_bounds__(1024) sort_colscan_kernel(PassArgs a, int coun
   }
   __syncthreads();
   unsigned run = part[g][dl];
-  if (d < ndig)
+  if (d < ndig && regs) {
+#pragma unroll
+    for (int k = 0; k < kR; ++k) {
+      if (t0 + k < t1) a.counts[(t0 + k) * ndig + d] = run;
+      run += r[k];
+    }
+  } else if (d < ndig)
     for (long long t = t0; t < t1; t += kU) {
       unsigned v[kU];
 #pragma unroll
@@ -266,8 +281,9 @@ __device__ __forceinline__ void digit_starts(const unsigned int* totals, int ndi
 // or a destination outside [0, m)) carry a flag; the last sub-pass neither
 // counts nor places them, so the valid records take ranks [0, valid count).
 // Counters are the 16-bit halves of 32-bit words: word (row r, thread t) at
-// r * T + t counts bucket r (low half) and bucket r + 16 (high half), so a
-// warp's counter accesses never share a bank.
+// r * T + t (swizzled like the records) counts bucket r (low half) and
+// bucket r + 16 (high half), so a warp's counter accesses never share a
+// bank.
 // Records live in shared memory as 32-bit words (flag << 31 | digit << 13 |
 // tile-local index) under an XOR swizzle of the 16-byte chunks in each
 // 128-byte line, so that the per-thread row reads are conflict-free.
@@ -363,7 +379,10 @@ template <int S, bool LAST>
 __device__ __forceinline__ void rank_subpass(unsigned (&rec)[kIPT], unsigned* __restrict__ recs,
                                              unsigned* __restrict__ cnt, unsigned* wsum) {
   const int T = blockDim.x, tid = threadIdx.x;
-  unsigned* col = cnt + tid;
+  // counter words take the records' swizzle: with T a multiple of 256,
+  // swz(r * T + t) = r * T + swz(t), so a thread's column stays one
+  // per-thread offset, and the scan's 16-word runs become conflict-free
+  unsigned* col = cnt + swz(tid);
   unsigned* spare = col + 16 * T;
 #pragma unroll
   for (int r = 0; r < 16; ++r) col[r * T] = 0u;
@@ -377,12 +396,13 @@ __device__ __forceinline__ void rank_subpass(unsigned (&rec)[kIPT], unsigned* __
   __syncthreads();
   // scan: thread t takes the words [16t, 16t + 16) of the row-major counter
   // matrix; the low halves (buckets < 16) all come before the high halves
-  uint4* run = reinterpret_cast<uint4*>(cnt) + 4 * tid;
+  uint4* run = reinterpret_cast<uint4*>(cnt);
+  const unsigned g0 = 4u * tid, gx = kSwizzle ? (g0 >> 3) & 7u : 0u;
   uint4 v[4];
   unsigned sum = 0;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    v[c] = run[c];
+    v[c] = run[(g0 + c) ^ gx];
     sum += v[c].x + v[c].y + v[c].z + v[c].w;
   }
   unsigned tot;
@@ -399,7 +419,7 @@ __device__ __forceinline__ void rank_subpass(unsigned (&rec)[kIPT], unsigned* __
     pre += v[c].z;
     o.w = pre;
     pre += v[c].w;
-    run[c] = o;
+    run[(g0 + c) ^ gx] = o;
   }
   __syncthreads();
 #pragma unroll
