@@ -593,9 +593,11 @@ __global__ void __launch_bounds__(512, 2) sort_pass_kernel(PassArgs a) {
   U* __restrict__ vout = reinterpret_cast<U*>(a.vals_out);
   const unsigned n32 = (unsigned)a.n;   // sort sizes are below 2^31
   bool bad = false;
+  // p = tid + kT with T a multiple of 256: swz(p) = p ^ xw for this thread
+  const unsigned xw = kSwizzle ? ((unsigned)(tid >> 5) & 7u) << 2 : 0u;
 #pragma unroll 4
   for (unsigned p = tid; p < nvalid_tile; p += T) {
-    const unsigned r = recs[swz(p)];
+    const unsigned r = recs[p ^ xw];
     const unsigned d = r >> kIdxBits, li = r & ((1u << kIdxBits) - 1u);
     const unsigned pos = off[d & mask] + p;
     // cannot fail for a correct ranking; never write out of bounds
@@ -751,8 +753,7 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
     if (lane == src) out[b * ostride] = out[b * ostride] + t;
   }
   // long groups: their blocks are reserved (the reservation order does not
-  // matter: a group's tree reads only its own nodes), then the warp writes
-  // the block list of its long groups one at a time
+  // matter: a group's tree reads only its own nodes) and listed
   const bool is_long = len > kMediumGroup;
   const long long nblk = is_long ? (len + kSegBlock - 1) / kSegBlock : 0;
   // one reservation per warp: exclusive prefixes of the block counts and of
@@ -783,7 +784,13 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
       set_status(status, DET_ERR_INVALID_ARG);
     }
   }
-  unsigned lng = __ballot_sync(0xffffffffu, reg);
+  // a group of at most 32 blocks writes its own list; the warp writes the
+  // lists of longer groups together, one group at a time
+  if (reg && nblk <= 32)
+    for (long long k = 0; k < nblk; ++k)
+      blocks[base + k] = BlockDesc{lo + k * kSegBlock, (unsigned)min((long long)kSegBlock, len - k * kSegBlock),
+                                   (unsigned)sidx};
+  unsigned lng = __ballot_sync(0xffffffffu, reg && nblk > 32);
   while (lng) {
     const int src = __ffs(lng) - 1;
     lng &= lng - 1;
