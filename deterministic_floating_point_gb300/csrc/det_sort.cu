@@ -813,7 +813,7 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
 // forms the PT over the bin's block nodes and adds it to out[bin]: who does
 // it varies, the tree does not.
 template <typename T, bool NEG>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, sizeof(T) == 8 ? 5 : 8)
 segtree_blocks_kernel(const T* __restrict__ vals, const BlockDesc* __restrict__ blocks,
                       const unsigned int* __restrict__ nblocks, const LongSeg* __restrict__ lsegs,
                       unsigned int* __restrict__ ldone, T* nodes, T* __restrict__ out, long long max_blocks,
@@ -828,18 +828,24 @@ segtree_blocks_kernel(const T* __restrict__ vals, const BlockDesc* __restrict__ 
   const BlockDesc B = blocks[q];
   if (B.sidx >= max_lsegs) return;
   const long long lo = B.lo, len = min((long long)kSegBlock, (long long)B.len);
+  // leaves sit in shared memory with the 16-byte chunks of each 128-byte
+  // line XOR-permuted by the line index, so that the per-thread reads of 8
+  // consecutive leaves are conflict-free
+  constexpr int EPC = 16 / (int)sizeof(T);   // leaves per 16-byte chunk
+  auto pchunk = [](int c) { return c ^ ((c >> 3) & 7); };
 #pragma unroll
   for (int i = 0; i < kSegBlock / 256; ++i) {
     const int j = i * 256 + tid;
-    buf[j] = j < len ? (NEG ? -__ldg(vals + lo + j) : __ldg(vals + lo + j)) : absent<T>();
+    buf[pchunk(j / EPC) * EPC + j % EPC] = j < len ? (NEG ? -__ldg(vals + lo + j) : __ldg(vals + lo + j)) : absent<T>();
   }
   __syncthreads();
   constexpr int NQ = 8 * (int)sizeof(T) / 16;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     float4 q4[NQ];
+    const int c0 = (h * (kSegBlock / 2) + tid * 8) / EPC;
 #pragma unroll
-    for (int i = 0; i < NQ; ++i) q4[i] = reinterpret_cast<const float4*>(buf + h * (kSegBlock / 2) + tid * 8)[i];
+    for (int i = 0; i < NQ; ++i) q4[i] = reinterpret_cast<const float4*>(buf)[pchunk(c0 + i)];
     T v[8];
     memcpy(v, q4, sizeof(v));
     const T node = warp_pt(thread_pt(v));
