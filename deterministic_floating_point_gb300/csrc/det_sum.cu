@@ -31,7 +31,9 @@ template <typename T> struct SumGeom {
 
 // PT over p[0..L) by a whole CTA; the result is returned to thread 0.
 // Thread t reduces the aligned group [t g, (t+1) g) with g = max(1, P / T)
-// (P = next power of two >= L) by an in-thread binary counter; the thread
+// (P = next power of two >= L): chunks of 8 leaves, their loads all in
+// flight, each reduced in registers (a level-3 node, absent terms past the
+// group or the end), the chunk nodes merged by a binary counter.  The thread
 // nodes are then reduced by warp_pt and a final PT over the warp nodes.
 template <typename T>
 __device__ T cta_pt_global(const T* p, long long L, T* smem_warp) {
@@ -41,28 +43,23 @@ __device__ T cta_pt_global(const T* p, long long L, T* smem_warp) {
   while (P < L) P <<= 1;
   long long g = P / nthreads;
   if (g < 1) g = 1;
-  T node = absent<T>();
+  T node;
   {
-    long long lo = (long long)tid * g;
-    T stack[40];
-    long long cnt = 0;
-    for (long long i = 0; i < g; ++i) {
-      long long idx = lo + i;
-      T v = (idx < L) ? __ldcg(p + idx) : absent<T>();
-      int lvl = 0;
-      long long c = cnt;
-      while (c & 1) {
-        v = stack[lvl] + v;
-        c >>= 1;
-        ++lvl;
+    const long long lo = (long long)tid * g;
+    NodeCounter<T, 6> nc;
+#pragma unroll 2
+    for (long long c = 0; c < g; c += 8) {
+      T v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const long long idx = lo + c + i;
+        v[i] = (c + i < g && idx < L) ? __ldcg(p + idx) : absent<T>();
       }
-      stack[lvl] = v;
-      ++cnt;
+      nc.push(thread_pt(v));
     }
-    // g is a power of two, so the counter ends with one full node
-    int top = 0;
-    while ((1LL << top) < g) ++top;
-    node = stack[top];
+    // g < 8: one chunk, PT over g leaves padded to 8; otherwise g / 8 (a
+    // power of two) chunk nodes, so the counter ends with one full node
+    node = nc.result();
   }
   node = warp_pt(node);
   if (lane == 0) smem_warp[warp] = node;
@@ -141,9 +138,12 @@ sum_kernel(const T* __restrict__ x, long long n, int tb_log2, long long ntiles, 
 }  // namespace
 
 // Tile size: a power of two number of 4 KB warp-blocks chosen from n only
-// (the bits do not depend on it; only the grid does).
+// (the bits do not depend on it; only the grid does).  Large inputs get
+// about 600 tiles (four or more CTAs per SM streaming); inputs below 4,800
+// warp-blocks get at least 128 larger tiles, so that the launch, the ticket
+// atomics and the final tree over the tile partials stay short.
 static int sum_tile_log2(long long nblocks) {
-  long long want = nblocks / 600;
+  long long want = nblocks >= 4800 ? nblocks / 600 : nblocks / 128;
   int t = 0;
   while (t < 10 && (2LL << t) <= want) ++t;
   return t;
