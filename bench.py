@@ -254,10 +254,11 @@ def build_workload(name, torch, det, dev):
             reps, secs = _timed_oracle(lambda: oracle.det_scatter_add_rows(out0_np, bins_np[:k], values_np[:k]))
             return k * W * reps, secs, f"{reps} x vec{W} scatter of the first {k} records, 1 thread"
 
-        # sort (key in, index out), gather (index in, W components in and out), W trees (W components in)
-        step_bytes = n * (4 + 4 + 4 + 2 * W * s + W * s) + 2 * m * W * s
+        # count (key in), pass (key and whole record in, W components out), W trees (W components in):
+        # the one-pass sort of records of at most 16 bytes carries the records itself
+        step_bytes = n * (4 + 4 + 2 * W * s + W * s) + 2 * m * W * s
         return dict(state={"out": out, "out0": torch.from_numpy(out0_np).to(dev), "b": b, "v": v}, step=step,
-                    elems=n * W, algo_bytes=n * (4 + 4), step_bytes=step_bytes, dominant="det_sort_pass",
+                    elems=n * W, algo_bytes=n * (4 + 2 * W * s), step_bytes=step_bytes, dominant="det_sort_pass",
                     dtype=dt, e2e_step=e2e_step, h2d=n * (4 + W * s), d2h=m * W * s, oracle_sample=oracle_sample,
                     config={"workload": f"det_scatter_add_vec n={n} vec{W} N(0,1) {dt}, {m} uniform bins, seed 6",
                             "n": n, "width": W, "bins": m, "l2": "L2 flushed between timed steps"})

@@ -45,6 +45,8 @@ struct PassArgs {
   unsigned int* n_valid;
   int32_t* seg_out;            // one-pass sorts: segment starts (m + 1), written by CTA 0 of the pass
   int32_t* rank_out;           // one-pass sorts: sorted position of every valid record, in input order
+  int width;                   // wide records: components per record (input row-major, output one
+  long long comp_stride;       // array per component, comp_stride elements apart)
 };
 
 // Digit of record i of a pass, or 0xffffffff if it is past the end or
@@ -436,7 +438,11 @@ __device__ __forceinline__ void rank_subpass(unsigned (&rec)[kIPT], unsigned* __
   if (!LAST) load_row(rec, recs);
 }
 
-template <int VB, bool FIRST, bool IDX, bool KEYS_OUT>
+// WIDE (one-pass sorts only): each record carries `width` components of VB
+// bytes, read as a row-major record array; the write-out puts component c of
+// sorted record p at vals_out[c * comp_stride + position], so each
+// component's groups come out contiguous for the segmented tree.
+template <int VB, bool FIRST, bool IDX, bool KEYS_OUT, bool WIDE = false>
 __global__ void __launch_bounds__(512, 2) sort_pass_kernel(PassArgs a) {
   using U = typename Payload<VB>::U;
   constexpr bool IDX_IN = IDX && !FIRST;                // input indices carried from the previous pass
@@ -447,7 +453,8 @@ __global__ void __launch_bounds__(512, 2) sort_pass_kernel(PassArgs a) {
   const int T = blockDim.x, tid = threadIdx.x;
   const int ndig = 1 << a.D;
   const unsigned mask = (unsigned)ndig - 1u;
-  const PassSmem L = pass_smem(T, ndig, VB, IDX_IN, KEYS_OUT);
+  const int W = WIDE ? a.width : 1;   // components per record
+  const PassSmem L = pass_smem(T, ndig, VB * W, IDX_IN, KEYS_OUT);
   unsigned* recs = reinterpret_cast<unsigned*>(smem_raw + L.recs);
   unsigned* rkeys = KEYS_OUT ? reinterpret_cast<unsigned*>(smem_raw + L.rkeys) : recs;
   U* sval = reinterpret_cast<U*>(smem_raw + L.vals);
@@ -465,21 +472,22 @@ __global__ void __launch_bounds__(512, 2) sort_pass_kernel(PassArgs a) {
   // ---- payloads (values, carried indices): one bulk copy each for a full,
   // aligned tile, landing while the keys are ranked; plain loads otherwise
   constexpr bool PAYLOAD = VB > 0 || IDX_IN;
-  const unsigned char* vsrc = reinterpret_cast<const unsigned char*>(a.vals_in) + tile_base * VB;
+  const unsigned char* vsrc = reinterpret_cast<const unsigned char*>(a.vals_in) + tile_base * VB * W;
   const int32_t* isrc = IDX_IN ? a.idx_in + tile_base : nullptr;
   const bool bulk = PAYLOAD && cn == K && (VB == 0 || (reinterpret_cast<uintptr_t>(vsrc) & 15) == 0) &&
                     (!IDX_IN || (reinterpret_cast<uintptr_t>(isrc) & 15) == 0);
   if (bulk && tid == 0) {
     mbar_init(&pay_bar, 1);
-    mbar_arrive_expect_tx(&pay_bar, (unsigned)(K * VB + (IDX_IN ? K * 4 : 0)));
-    if (VB) bulk_copy_g2s(sval, vsrc, (unsigned)(K * VB), &pay_bar);
+    mbar_arrive_expect_tx(&pay_bar, (unsigned)(K * VB * W + (IDX_IN ? K * 4 : 0)));
+    if (VB) bulk_copy_g2s(sval, vsrc, (unsigned)(K * VB * W), &pay_bar);
     if (IDX_IN) bulk_copy_g2s(sidx, isrc, (unsigned)(K * 4), &pay_bar);
   }
-  if (PAYLOAD && !bulk)
-    for (int p = tid; p < cn; p += T) {
+  if (PAYLOAD && !bulk) {
+    for (int p = tid; p < cn * W; p += T)
       if (VB) sval[p] = __ldg(reinterpret_cast<const U*>(vsrc) + p);
-      if (IDX_IN) sidx[p] = __ldg(isrc + p);
-    }
+    if (IDX_IN)
+      for (int p = tid; p < cn; p += T) sidx[p] = __ldg(isrc + p);
+  }
 
   // ---- raw keys into the swizzled record array: 16-byte asynchronous
   // copies for a full, aligned tile (32 KB in flight per CTA), completed
@@ -605,7 +613,11 @@ __global__ void __launch_bounds__(512, 2) sort_pass_kernel(PassArgs a) {
     bad |= !ok;
     if (ok) {
       if (RANK) a.rank_out[tile_base + li] = (int32_t)pos;
-      if (VB) vout[pos] = sval[li];
+      if (WIDE) {
+        for (int c = 0; c < W; ++c) vout[c * a.comp_stride + pos] = sval[li * W + c];
+      } else if (VB) {
+        vout[pos] = sval[li];
+      }
       if (IDX) a.idx_out[pos] = IDX_IN ? sidx[li] : (int32_t)(tile_base + li);
       if (KEYS_OUT) {
         const int32_t k = (int32_t)rkeys[swz(li)];
@@ -956,12 +968,13 @@ SortPlan make_sort_plan(long long n, long long m, int value_bytes, bool need_idx
 
 template <int VB>
 static cudaError_t launch_pass(const PassArgs& a, bool first, bool idx, bool keys_out, int threads, long long tiles,
-                               cudaStream_t s) {
+                               cudaStream_t s, bool wide = false) {
   const int ndig = 1 << a.D;
-  const size_t smem = pass_smem(threads, ndig, VB, idx && !first, keys_out).total;
+  const size_t smem = pass_smem(threads, ndig, VB * (wide ? a.width : 1), idx && !first, keys_out).total;
   void (*k)(PassArgs) = nullptr;
+  if (wide) k = sort_pass_kernel<VB, true, false, false, true>;
 #define DET_PICK(F, I, KO) \
-  if (first == F && idx == I && keys_out == KO) k = sort_pass_kernel<VB, F, I, KO>;
+  if (!wide && first == F && idx == I && keys_out == KO) k = sort_pass_kernel<VB, F, I, KO>;
   DET_PICK(true, true, true) DET_PICK(true, true, false) DET_PICK(true, false, true) DET_PICK(true, false, false)
   DET_PICK(false, true, true) DET_PICK(false, true, false) DET_PICK(false, false, true) DET_PICK(false, false, false)
 #undef DET_PICK
@@ -974,7 +987,7 @@ static cudaError_t launch_pass(const PassArgs& a, bool first, bool idx, bool key
 }
 
 int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key_offset, const void* values,
-                 int32_t* perm_out, cudaStream_t s, int* final_buf, int32_t* rank_out) {
+                 int32_t* perm_out, cudaStream_t s, int* final_buf, int32_t* rank_out, void* comp_out) {
   char* w = reinterpret_cast<char*>(ws);
   SortHdr* h = reinterpret_cast<SortHdr*>(ws);
   if (cudaMemsetAsync(w, 0, kHeaderBytes, s) != cudaSuccess) return DET_ERR_CUDA;
@@ -1010,6 +1023,13 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
     a.n_valid = &h->n_valid;
     a.seg_out = p.passes == 1 ? seg : nullptr;
     a.rank_out = p.passes == 1 ? rank_out : nullptr;
+    a.width = 1;
+    a.comp_stride = 0;
+    if (p.wide) {   // one-pass plans only: whole records into one array per component
+      a.vals_out = comp_out;
+      a.width = p.wide;
+      a.comp_stride = p.n;
+    }
     const size_t csmem = align_up((size_t)(ndig + 1) * 4, 16) + (size_t)p.threads * kIPT * 4;
     const long long K = (long long)p.threads * kIPT;
     void (*ck)(PassArgs, long long) = first ? sort_count_kernel<true> : sort_count_kernel<false>;
@@ -1025,7 +1045,10 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
     if (rc != DET_OK) return rc;
     const bool keys_out = p.passes > 1;
     cudaError_t e;
-    if (p.value_bytes == 8)
+    if (p.wide)
+      e = p.wide_elem == 8 ? launch_pass<8>(a, true, false, false, p.threads, p.tiles, s, true)
+                           : launch_pass<4>(a, true, false, false, p.threads, p.tiles, s, true);
+    else if (p.value_bytes == 8)
       e = launch_pass<8>(a, first, p.need_idx, keys_out, p.threads, p.tiles, s);
     else if (p.value_bytes == 4)
       e = launch_pass<4>(a, first, p.need_idx, keys_out, p.threads, p.tiles, s);

@@ -30,6 +30,10 @@ struct SortPlan {
   size_t totals = 0, counts = 0, keys[2] = {0, 0}, vals[2] = {0, 0}, idx[2] = {0, 0};
   size_t seg = 0, blocks = 0, lsegs = 0, ldone = 0, nodes = 0, total = 0;
   long long max_blocks = 0, max_lsegs = 0;
+  // Wide records (set by the caller on a one-pass plan without values or
+  // indices): `wide` components of wide_elem bytes per record, moved by the
+  // pass into one array per component (enqueue_sort's comp_out).
+  int wide = 0, wide_elem = 0;
 };
 
 // Header fields of a sort workspace (overlays the first 256 bytes).
@@ -50,8 +54,11 @@ SortPlan make_sort_plan(long long n, long long m, int value_bytes, bool need_idx
 // at plan.seg.  With rank_out (one-pass plans without values or indices
 // only) the pass writes each valid record's sorted position to rank_out[i],
 // in input order, and moves nothing else.  Returns DET_OK or DET_ERR_CUDA.
+// With plan.wide, the values are row-major records and component c of the
+// record at sorted position q goes to comp_out[c * n + q].
 int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key_offset, const void* values,
-                 int32_t* perm_out, cudaStream_t s, int* final_buf, int32_t* rank_out = nullptr);
+                 int32_t* perm_out, cudaStream_t s, int* final_buf, int32_t* rank_out = nullptr,
+                 void* comp_out = nullptr);
 
 // Segmented pairwise tree: out[b] = out[b] + PT(vals[seg[b] .. seg[b+1]))
 // for every non-empty b.  T is float or double.

@@ -3,9 +3,11 @@
 // Warp user guide "Deterministic Execution", "Pattern 1: Accumulation":
 // vectors, matrices, quaternions and transforms take the same segmented
 // reduction path as scalars, component by component.  Here: one stable sort
-// of the records by destination (the record index as payload), one gather
-// that lays each component out in sorted order, then per component the
-// scalar segmented tree: out[b][c] = out[b][c] + PT(component c of group b).
+// of the records by destination that lays each component out in sorted
+// order, then per component the scalar segmented tree:
+// out[b][c] = out[b][c] + PT(component c of group b).  A one-pass sort of
+// records of at most 16 bytes carries the whole record through the pass;
+// otherwise the sort carries the record index and a gather follows.
 #include "det_sort.cuh"
 
 #include <algorithm>
@@ -46,13 +48,27 @@ int vec_impl(T* out, long long m, long long width, const int32_t* bins, const T*
   if (ws_bytes < L.total) return DET_ERR_WORKSPACE;
   if (n == 0 || m == 0 || width == 0)
     return cudaMemsetAsync(ws, 0, kHeaderBytes, s) == cudaSuccess ? DET_OK : DET_ERR_CUDA;
-  const SortPlan& p = L.plan;
-  int fb = 0;
-  int rc = enqueue_sort(p, ws, bins, 0, nullptr, nullptr, s, &fb);
-  if (rc != DET_OK) return rc;
   char* w = reinterpret_cast<char*>(ws);
   SortHdr* h = reinterpret_cast<SortHdr*>(ws);
   T* comp = reinterpret_cast<T*>(w + L.comp);
+  int fb = 0;
+  SortPlan q = make_sort_plan(n, m, 0, false, 128);   // tiles of 4,096: the records fill shared memory
+  if (q.passes == 1 && width * (long long)sizeof(T) <= 16 && q.total <= L.comp) {
+    // records through the pass: no index, no gather (the plan's workspace
+    // ends before the component arrays at L.comp)
+    q.wide = (int)width;
+    q.wide_elem = (int)sizeof(T);
+    int rc = enqueue_sort(q, ws, bins, 0, values, nullptr, s, &fb, nullptr, comp);
+    if (rc != DET_OK) return rc;
+    for (long long c = 0; c < width; ++c) {
+      rc = enqueue_segmented_tree<T>(q, ws, comp + c * n, out + c, s, false, width, c > 0);
+      if (rc != DET_OK) return rc;
+    }
+    return DET_OK;
+  }
+  const SortPlan& p = L.plan;
+  int rc = enqueue_sort(p, ws, bins, 0, nullptr, nullptr, s, &fb);
+  if (rc != DET_OK) return rc;
   // one thread per record: many independent gathers in flight
   const long long grid = std::max(1LL, (long long)((n + 255) / 256));
   launch_begin("det_vec_gather", s);
