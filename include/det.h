@@ -26,8 +26,9 @@
  *   CUDA graph.
  * - `block_threads` selects the CUDA block size: 0 (the default) or one of
  *   128, 256, 512, 1024.  It changes the launch shape only, never the bits.
- *   The sorts behind the scatter calls use 128-thread CTAs when asked for
- *   128 and 256-thread CTAs otherwise.
+ *   The sorts behind the scatter calls sort tiles of 4,096 records (CTAs of
+ *   256 threads) when asked for 128 and tiles of 8,192 (CTAs of 512)
+ *   for 256, 512 or 1024; by default they pick the tile from the sizes.
  * - Return value: DET_OK, or an error code for a bad argument found on the
  *   host (nothing is enqueued then), or DET_ERR_CUDA if a launch failed.
  *   Errors detected on the device (a look-back wait that gave up) are written
