@@ -13,11 +13,10 @@
 //             stable, so after the last pass each destination's records are
 //             in ascending original index.
 //   bounds    (more than one pass) segment starts from the sorted keys
-//   tree      out[b] = out[b] + PT(group b): groups of at most 32 records
-//             by one thread, of at most 1024 by one warp; longer groups are
-//             cut into rank-aligned 4096-blocks (subtrees of the group's
-//             tree), reduced by one CTA each, then a tree over the block
-//             nodes.
+//   tree      out[b] = out[b] + PT(group b): groups of at most 1024 records
+//             by one thread; longer groups are cut into rank-aligned
+//             4096-blocks (subtrees of the group's tree), reduced by one CTA
+//             each, then a tree over the block nodes.
 #include "det_sort.cuh"
 
 namespace det {
@@ -629,31 +628,39 @@ __global__ void __launch_bounds__(512, 2) sort_pass_kernel(PassArgs a) {
 }
 
 // seg[b] = first sorted position with key >= b, for b = 0..m (keys sorted).
-// Thread t covers positions [4t, 4t + 4) -- four keys by one 16-byte load --
-// and, for the thread that reaches it, position N (the valid count), where
-// every remaining bin starts.
+// Thread t covers positions [P t, P t + P) -- P keys by 16-byte loads, all
+// in flight (P = 16 for large sorts, 4 for smaller ones, which need the
+// threads) -- and, for the thread that reaches it, position N (the valid
+// count), where every remaining bin starts.
+template <int kBoundsPer>
 __global__ void sort_bounds_kernel(const int32_t* __restrict__ keys, const unsigned int* __restrict__ n_valid,
                                    long long m, int32_t* __restrict__ seg, long long n) {
-  const long long i0 = 4 * ((long long)blockIdx.x * blockDim.x + threadIdx.x);
+  const long long i0 = kBoundsPer * ((long long)blockIdx.x * blockDim.x + threadIdx.x);
   const long long N = min((long long)*n_valid, n);
   if (i0 > N) return;
   auto clampk = [&](int32_t k) { return max(-1LL, min((long long)k, m)); };
-  long long k[5];   // k[0]: the key before i0; k[1 + e]: the key at i0 + e (m from N on)
-  k[0] = i0 == 0 ? -1 : clampk(__ldg(keys + i0 - 1));
-  if (i0 + 4 <= N && (reinterpret_cast<uintptr_t>(keys + i0) & 15) == 0) {
-    const int4 q = __ldg(reinterpret_cast<const int4*>(keys + i0));
-    k[1] = clampk(q.x);
-    k[2] = clampk(q.y);
-    k[3] = clampk(q.z);
-    k[4] = clampk(q.w);
+  int32_t kr[kBoundsPer];   // the keys at i0 + e (m from N on)
+  const long long before = i0 == 0 ? -1 : clampk(__ldg(keys + i0 - 1));
+  if (i0 + kBoundsPer <= N && (reinterpret_cast<uintptr_t>(keys + i0) & 15) == 0) {
+#pragma unroll
+    for (int q = 0; q < kBoundsPer / 4; ++q) {
+      const int4 v = __ldg(reinterpret_cast<const int4*>(keys + i0) + q);
+      kr[4 * q] = v.x;
+      kr[4 * q + 1] = v.y;
+      kr[4 * q + 2] = v.z;
+      kr[4 * q + 3] = v.w;
+    }
   } else {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) k[1 + e] = i0 + e < N ? clampk(__ldg(keys + i0 + e)) : m;
+    for (int e = 0; e < kBoundsPer; ++e) kr[e] = i0 + e < N ? __ldg(keys + i0 + e) : 0;
   }
+  long long prev = before;
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
+  for (int e = 0; e < kBoundsPer; ++e) {
     if (i0 + e > N) break;
-    for (long long b = k[e] + 1; b <= k[e + 1]; ++b) seg[b] = (int32_t)(i0 + e);
+    const long long cur = i0 + e < N ? clampk(kr[e]) : m;
+    for (long long b = prev + 1; b <= cur; ++b) seg[b] = (int32_t)(i0 + e);
+    prev = cur;
   }
 }
 
@@ -699,7 +706,7 @@ struct BlockDesc {
   unsigned int sidx;   // the bin's entry in the long-segment list
 };
 
-constexpr int kMediumGroup = 1024;   // groups up to this size are reduced by one warp
+constexpr int kMediumGroup = 1024;   // groups up to this size are reduced by one thread; longer ones by blocks
 
 // Leaves [0, W) of a short group by one thread: the group's len <= W values
 // (negated for NEG) padded with absent terms, then the in-register tree --
@@ -720,8 +727,8 @@ __device__ __forceinline__ T thread_group_pt(const T* __restrict__ p, long long 
 }
 
 // One thread per bin b: out[b] = out[b] + PT(group b).
-//   groups of at most 32 records: the thread's own in-register tree
-//   up to kMediumGroup records: the whole warp, one such group at a time
+//   up to kMediumGroup records: the thread's own in-register trees over
+//     128-byte chunks of leaves, merged by a counter
 //   longer groups: cut into rank-aligned 4096-blocks (subtrees of the
 //     group's tree) for the block kernel; the warp writes their list
 // NEG: the tree is over the negated values (scatter-sub).  The leaves are
@@ -743,26 +750,15 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
     lo = max(0LL, min((long long)seg[b], hi));
     len = hi - lo;
   }
-  if (len > 0 && len <= 32) {
-    T t;
-    if (len <= 4)
-      t = thread_group_pt<T, NEG, 4>(vals + lo, len);
-    else if (len <= 8)
-      t = thread_group_pt<T, NEG, 8>(vals + lo, len);
-    else if (len <= 16)
-      t = thread_group_pt<T, NEG, 16>(vals + lo, len);
-    else
-      t = thread_group_pt<T, NEG, 32>(vals + lo, len);
-    out[b * ostride] = out[b * ostride] + t;
-  }
-  // the warp's medium groups, one at a time
-  unsigned med = __ballot_sync(0xffffffffu, len > 32 && len <= kMediumGroup);
-  while (med) {
-    const int src = __ffs(med) - 1;
-    med &= med - 1;
-    const long long mlo = __shfl_sync(0xffffffffu, lo, src), mlen = __shfl_sync(0xffffffffu, len, src);
-    const T t = warp_pt_range<T, false, NEG>(vals + mlo, mlen);
-    if (lane == src) out[b * ostride] = out[b * ostride] + t;
+  if (len > 0 && len <= kMediumGroup) {
+    // rank-aligned chunks of 128 bytes of leaves (level-5 nodes for f32,
+    // level-4 for f64; absent terms past the group) merged by a binary
+    // counter.  Neighbouring bins have similar sizes in practice, so the
+    // lanes of a warp mostly run the same number of chunks.
+    constexpr int CW = 128 / (int)sizeof(T);
+    NodeCounter<T, 6> nc;
+    for (long long c = 0; c < len; c += CW) nc.push(thread_group_pt<T, NEG, CW>(vals + lo + c, len - c));
+    out[b * ostride] = out[b * ostride] + nc.result();
   }
   // long groups: their blocks are reserved (the reservation order does not
   // matter: a group's tree reads only its own nodes) and listed
@@ -1058,8 +1054,11 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
   }
   if (p.passes > 1) {   // one-pass sorts got their segment starts from the pass
     launch_begin("det_sort_bounds", s);
-    sort_bounds_kernel<<<(unsigned)((p.n + 1 + 1023) / 1024), 256, 0, s>>>(
-        reinterpret_cast<const int32_t*>(w + p.keys[*final_buf]), &h->n_valid, p.m, seg, p.n);
+    const int32_t* fkeys = reinterpret_cast<const int32_t*>(w + p.keys[*final_buf]);
+    if (p.n > (1LL << 24))
+      sort_bounds_kernel<16><<<(unsigned)((p.n + 1 + 4095) / 4096), 256, 0, s>>>(fkeys, &h->n_valid, p.m, seg, p.n);
+    else
+      sort_bounds_kernel<4><<<(unsigned)((p.n + 1 + 1023) / 1024), 256, 0, s>>>(fkeys, &h->n_valid, p.m, seg, p.n);
     launch_end(s);
   }
   return check_launch("sort: segment starts");
