@@ -48,25 +48,6 @@ struct PassArgs {
   long long comp_stride;       // array per component, comp_stride elements apart)
 };
 
-// Digit of record i of a pass, or 0xffffffff if it is past the end or
-// (first pass) its destination is outside [0, m).
-// The count kernel reads the keys with a normal cached load so that the
-// pass kernel, which reads them last, mostly finds them in L2.
-template <bool FIRST>
-__device__ __forceinline__ unsigned digit_of(const PassArgs& a, int32_t raw, unsigned mask) {
-  if (FIRST) {
-    if (a.key_offset == 0) return (unsigned)raw < (unsigned long long)a.m ? ((unsigned)raw >> a.shift) & mask : 0xffffffffu;
-    const long long k = (long long)raw + a.key_offset;
-    return (k >= 0 && k < a.m) ? ((unsigned)k >> a.shift) & mask : 0xffffffffu;
-  }
-  return ((unsigned)raw >> a.shift) & mask;
-}
-template <bool FIRST, bool LAST_USE>
-__device__ __forceinline__ unsigned record_digit(const PassArgs& a, long long i, long long N, unsigned mask) {
-  if (i >= N) return 0xffffffffu;
-  return digit_of<FIRST>(a, LAST_USE ? __ldcs(a.keys_in + i) : __ldg(a.keys_in + i), mask);
-}
-
 // counts[tile][d] = records of the tile with digit d.  The tile is the
 // scatter pass's tile (K = pass_threads * kIPT records).  A full, aligned
 // tile's keys come in by one bulk copy into shared memory (32 KB in flight
