@@ -459,8 +459,10 @@ __global__ void __launch_bounds__(512, 2) sort_pass_kernel(PassArgs a) {
   if (bulk && tid == 0) {
     mbar_init(&pay_bar, 1);
     mbar_arrive_expect_tx(&pay_bar, (unsigned)(K * VB * W + (IDX_IN ? K * 4 : 0)));
-    if (VB) bulk_copy_g2s(sval, vsrc, (unsigned)(K * VB * W), &pay_bar);
-    if (IDX_IN) bulk_copy_g2s(sidx, isrc, (unsigned)(K * 4), &pay_bar);
+    // read for the last time: leave L2 to the sorted output, which the trees read next
+    const unsigned long long pol = l2_evict_first();
+    if (VB) bulk_copy_g2s_hint(sval, vsrc, (unsigned)(K * VB * W), &pay_bar, pol);
+    if (IDX_IN) bulk_copy_g2s_hint(sidx, isrc, (unsigned)(K * 4), &pay_bar, pol);
   }
   if (PAYLOAD && !bulk) {
     for (int p = tid; p < cn * W; p += T)
@@ -475,9 +477,10 @@ __global__ void __launch_bounds__(512, 2) sort_pass_kernel(PassArgs a) {
   const int32_t* ksrc = a.keys_in + tile_base;
   const bool kasync = cn == K && (reinterpret_cast<uintptr_t>(ksrc) & 15) == 0;
   if (kasync) {
+    const unsigned long long kpol = l2_evict_first();   // the keys' last read
     for (int g = tid; g < (int)(K / 4); g += T)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(rkeys + swz(4u * g))),
-                   "l"(ksrc + 4 * g)
+      asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(rkeys + swz(4u * g))),
+                   "l"(ksrc + 4 * g), "l"(kpol)
                    : "memory");
     asm volatile("cp.async.commit_group;" ::: "memory");
   } else {
