@@ -55,7 +55,9 @@ struct PassArgs {
 // shared atomics (dropped keys into a spare slot).  A group of four keys
 // that is one digit across the whole warp is added by lane 0 alone: a hot
 // digit would otherwise serialise the warp's atomics on one address.
-template <bool FIRST>
+// OFFSET (first pass only): keys are shifted by key_offset before the range
+// test.  The first pass takes the lowest digit, so it never shifts.
+template <bool FIRST, bool OFFSET>
 __global__ void __launch_bounds__(256) sort_count_kernel(PassArgs a, long long K) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ __align__(8) unsigned long long keys_bar;
@@ -75,14 +77,13 @@ __global__ void __launch_bounds__(256) sort_count_kernel(PassArgs a, long long K
   }
   for (int d = tid; d <= ndig; d += blockDim.x) cnt[d] = 0u;
   __syncthreads();
-  const bool plain = !FIRST || a.key_offset == 0;
   const unsigned m32 = (unsigned)min(a.m, (long long)0x80000000LL);   // keys are int32
   const int shift = a.shift;
   auto digit = [&](int k) -> unsigned {
+    if (FIRST && !OFFSET) return (unsigned)k < m32 ? (unsigned)k & mask : (unsigned)ndig;
     if (FIRST) {
-      if (plain) return (unsigned)k < m32 ? ((unsigned)k >> shift) & mask : (unsigned)ndig;
       const long long kk = (long long)k + a.key_offset;
-      return (kk >= 0 && kk < a.m) ? ((unsigned)kk >> shift) & mask : (unsigned)ndig;
+      return (kk >= 0 && kk < a.m) ? (unsigned)kk & mask : (unsigned)ndig;
     }
     return ((unsigned)k >> shift) & mask;
   };
@@ -553,7 +554,7 @@ __global__ void __launch_bounds__(512, 2) sort_pass_kernel(PassArgs a) {
           kk = (unsigned)o;
         }
       }
-      const unsigned d = (kk >> a.shift) & mask;
+      const unsigned d = (FIRST ? kk : kk >> a.shift) & mask;   // the first pass takes the lowest digit
       rec[j] = ok ? (d << kIdxBits) | li : kDropped | li;
     }
   }
@@ -1012,7 +1013,9 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
     }
     const size_t csmem = align_up((size_t)(ndig + 1) * 4, 16) + (size_t)p.threads * kIPT * 4;
     const long long K = (long long)p.threads * kIPT;
-    void (*ck)(PassArgs, long long) = first ? sort_count_kernel<true> : sort_count_kernel<false>;
+    void (*ck)(PassArgs, long long) = !first            ? sort_count_kernel<false, false>
+                                      : key_offset == 0 ? sort_count_kernel<true, false>
+                                                        : sort_count_kernel<true, true>;
     const cudaError_t ce = ensure_dyn_smem((const void*)ck, csmem);
     if (ce != cudaSuccess) return cuda_fail(ce, "sort: digit counts");
     launch_begin("det_sort_count", s);
