@@ -722,7 +722,7 @@ __device__ __forceinline__ T thread_group_pt(const T* __restrict__ p, long long 
 template <typename T, bool NEG>
 __global__ void __launch_bounds__(256)
 segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg, long long m, T* __restrict__ out,
-                    BlockDesc* __restrict__ blocks, LongSeg* __restrict__ lsegs, unsigned int* __restrict__ ldone,
+                    BlockDesc* __restrict__ blocks, LongSeg* __restrict__ lsegs,
                     unsigned int* __restrict__ nblocks, unsigned int* __restrict__ nlsegs,
                     const unsigned int* __restrict__ n_valid, long long max_blocks, long long max_lsegs,
                     unsigned int* __restrict__ status, long long ostride) {
@@ -772,7 +772,6 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
     reg = sidx < max_lsegs && base + nblk <= max_blocks;
     if (reg) {
       lsegs[sidx] = LongSeg{b, base, nblk};
-      ldone[sidx] = 0u;
     } else {
       set_status(status, DET_ERR_INVALID_ARG);
     }
@@ -802,19 +801,16 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
 // 2048-record half (a level-3 node), the warp's butterfly gives the level-8
 // node, the tree over the 8 warps the level-11 node and the two halves the
 // level-12 node -- the same node as any other aligned decomposition of the
-// block.  The CTA that completes a bin's last block (a per-bin counter)
-// forms the PT over the bin's block nodes and adds it to out[bin]: who does
-// it varies, the tree does not.
+// block.  A second launch forms the PT over each bin's block nodes and adds
+// it to out[bin].
 template <typename T, bool NEG>
 __global__ void __launch_bounds__(256, sizeof(T) == 8 ? 5 : 8)
 segtree_blocks_kernel(const T* __restrict__ vals, const BlockDesc* __restrict__ blocks,
-                      const unsigned int* __restrict__ nblocks, const LongSeg* __restrict__ lsegs,
-                      unsigned int* __restrict__ ldone, T* nodes, T* __restrict__ out, long long max_blocks,
-                      long long max_lsegs, long long ostride) {
+                      const unsigned int* __restrict__ nblocks, T* __restrict__ nodes, long long max_blocks,
+                      long long max_lsegs) {
   static_assert(kSegBlock == 2 * 256 * 8, "one CTA of 256 threads x 8 leaves per half block");
   __shared__ __align__(16) T buf[kSegBlock];
   __shared__ T wnode[2][8];
-  __shared__ int last;
   const long long q = blockIdx.x;
   if (q >= (long long)*nblocks || q >= max_blocks) return;
   const int tid = threadIdx.x;
@@ -854,16 +850,21 @@ segtree_blocks_kernel(const T* __restrict__ vals, const BlockDesc* __restrict__ 
       half[h] = (a01 + a23) + (a45 + a67);
     }
     nodes[q] = half[0] + half[1];
-    __threadfence();
-    last = atomicAdd(&ldone[B.sidx], 1u) == (unsigned)(lsegs[B.sidx].nblk - 1);
   }
-  __syncthreads();
-  if (last && tid < 32) {
-    __threadfence();
-    const LongSeg L = lsegs[B.sidx];
-    const T t = warp_pt_range<T, true>(nodes + L.base, L.nblk);   // nodes already hold the negated leaves
-    if (tid == 0) out[L.bin * ostride] = out[L.bin * ostride] + t;
-  }
+}
+
+// One warp per long bin: the PT over the bin's block nodes (in block order,
+// absent padding), added to out[bin].  The block nodes come from the
+// previous launch.
+template <typename T>
+__global__ void __launch_bounds__(256)
+segtree_finish_kernel(const LongSeg* __restrict__ lsegs, const unsigned int* __restrict__ nlsegs,
+                      const T* __restrict__ nodes, T* __restrict__ out, long long max_lsegs, long long ostride) {
+  const long long sidx = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (sidx >= min((long long)*nlsegs, max_lsegs)) return;
+  const LongSeg L = lsegs[sidx];
+  const T t = warp_pt_range<T>(nodes + L.base, L.nblk);   // nodes already hold the negated leaves
+  if ((threadIdx.x & 31) == 0) out[L.bin * ostride] = out[L.bin * ostride] + t;
 }
 
 }  // namespace
@@ -939,8 +940,6 @@ SortPlan make_sort_plan(long long n, long long m, int value_bytes, bool need_idx
   off = align_up(off + (size_t)p.max_blocks * sizeof(BlockDesc), 256);
   p.lsegs = off;
   off = align_up(off + (size_t)p.max_lsegs * sizeof(LongSeg), 256);
-  p.ldone = off;
-  off = align_up(off + (size_t)p.max_lsegs * 4, 256);
   p.nodes = off;
   off = align_up(off + (size_t)p.max_blocks * 8, 256);
   p.total = off;
@@ -1061,12 +1060,11 @@ int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T*
   BlockDesc* blocks = reinterpret_cast<BlockDesc*>(w + p.blocks);
   LongSeg* lsegs = reinterpret_cast<LongSeg*>(w + p.lsegs);
   T* nodes = reinterpret_cast<T*>(w + p.nodes);
-  unsigned int* ldone = reinterpret_cast<unsigned int*>(w + p.ldone);
   if (reset_counters && cudaMemsetAsync(&h->long_blocks, 0, 2 * sizeof(unsigned int), s) != cudaSuccess)
     return DET_ERR_CUDA;
   launch_begin("det_segtree_bins", s);
   auto* kb = negate ? segtree_bins_kernel<T, true> : segtree_bins_kernel<T, false>;
-  kb<<<(unsigned)((p.m + 255) / 256), 256, 0, s>>>(sorted_vals, seg, p.m, out, blocks, lsegs, ldone,
+  kb<<<(unsigned)((p.m + 255) / 256), 256, 0, s>>>(sorted_vals, seg, p.m, out, blocks, lsegs,
                                                          &h->long_blocks, &h->long_segs, &h->n_valid, p.max_blocks,
                                                          p.max_lsegs, &h->status, ostride);
   launch_end(s);
@@ -1074,10 +1072,16 @@ int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T*
   if (rc != DET_OK) return rc;
   launch_begin("det_segtree_blocks", s);
   auto* kk = negate ? segtree_blocks_kernel<T, true> : segtree_blocks_kernel<T, false>;
-  kk<<<(unsigned)p.max_blocks, 256, 0, s>>>(sorted_vals, blocks, &h->long_blocks, lsegs, ldone, nodes, out,
-                                            p.max_blocks, p.max_lsegs, ostride);
+  kk<<<(unsigned)p.max_blocks, 256, 0, s>>>(sorted_vals, blocks, &h->long_blocks, nodes, p.max_blocks,
+                                            p.max_lsegs);
   launch_end(s);
-  return check_launch("segmented tree: blocks");
+  const int rc2 = check_launch("segmented tree: blocks");
+  if (rc2 != DET_OK) return rc2;
+  launch_begin("det_segtree_finish", s);
+  segtree_finish_kernel<T><<<(unsigned)((p.max_lsegs * 32 + 255) / 256), 256, 0, s>>>(lsegs, &h->long_segs, nodes, out,
+                                                                                    p.max_lsegs, ostride);
+  launch_end(s);
+  return check_launch("segmented tree: finish");
 }
 
 template int enqueue_segmented_tree<float>(const SortPlan&, void*, const float*, float*, cudaStream_t, bool, long long,

@@ -28,7 +28,7 @@ struct SortPlan {
   bool need_idx = false;    // carry the original index
   // workspace offsets (bytes from the workspace start)
   size_t totals = 0, counts = 0, keys[2] = {0, 0}, vals[2] = {0, 0}, idx[2] = {0, 0};
-  size_t seg = 0, blocks = 0, lsegs = 0, ldone = 0, nodes = 0, total = 0;
+  size_t seg = 0, blocks = 0, lsegs = 0, nodes = 0, total = 0;
   long long max_blocks = 0, max_lsegs = 0;
   // Wide records (set by the caller on a one-pass plan without values or
   // indices): `wide` components of wide_elem bytes per record, moved by the
