@@ -480,6 +480,81 @@ def test_scan_fingerprint_after_anchor(dtype):
 
 
 @pytest.mark.parametrize("dtype", [F32, F64])
+def test_scan_fingerprint_element_fold_after_carry(dtype):
+    """The element step.  Lane 0 of warp 1 holds b then c, and its carry is
+    the warp prefix WX[1] = a.  Each element is the running fold that starts
+    from the carry, so the second one is ((a+b)+c), not the carry plus the
+    lane's own prefix, (a+(b+c))."""
+    E, C = scan_geometry(dtype)
+    spots = {"a": 0, "b": 32 * E, "c": 32 * E + 1}
+    _fingerprint_case(dtype, C, E, spots, 32 * E + 1, "((a+b)+c)", 6)
+
+
+@pytest.mark.parametrize("dtype", [F32, F64])
+def test_scan_fingerprint_element_fold_full_carry(dtype):
+    """Chunk 1, warp 5, lane 3 holds d (element 0) and e (element 2).  Its
+    carry is ((Excl(1) + WX[5]) + LX[3]) with Excl(1) = a (chunk 0),
+    WX[5] = b (warp 3 of chunk 1) and LX[3] = c (lane 2 of warp 5); d and e
+    are then folded in one at a time: ((((a+b)+c)+d)+e), where the
+    carry-plus-lane-prefix form would give (((a+b)+c)+(d+e))."""
+    E, C = scan_geometry(dtype)
+    w5 = C + 5 * 32 * E
+    spots = {"a": 7, "b": C + 3 * 32 * E + 1, "c": w5 + 2 * E + 4,
+             "d": w5 + 3 * E, "e": w5 + 3 * E + 2}
+    _fingerprint_case(dtype, C, E, spots, w5 + 3 * E + 2, "((((a+b)+c)+d)+e)", 7)
+
+
+def _segmented_fingerprint_case(dtype, E, offsets, outside, spots, query, bracket, seed):
+    """Like _fingerprint_case for det_segmented_scan: ``outside`` holds
+    positions before the query's segment head, filled with large values that
+    must not reach the result."""
+    rng = np.random.default_rng(seed)
+    order = sorted(spots, key=lambda nm: spots[nm])
+    vals = distinguishing_values(order, dtype, rng, canonical(parse(bracket), order))
+    n = int(offsets[-1])
+    x = np.full(n, -0.0, dtype)
+    for p in outside:
+        x[p] = dtype(1024.0 + p)
+    for nm, p in spots.items():
+        x[p] = vals[nm]
+    y = oracle.det_segmented_scan(x, np.asarray(offsets, np.int64))
+    assert same_bits(y[query], evaluate(parse(bracket), vals, dtype)), (bracket, y[query])
+    hits = [t for t in all_trees(order) if same_bits(evaluate(t, vals, dtype), y[query])]
+    assert len(hits) == 1
+
+
+@pytest.mark.parametrize("dtype", [F32, F64])
+def test_segscan_fingerprint_element_fold_full_carry(dtype):
+    """The segmented element step.  The segment starts at element 3 of chunk
+    0 (a); chunk 0's element 1 (before the head) is large and must vanish.
+    In chunk 1, b sits in warp 2 and c in lane 1 of warp 4; lane 2 of warp 4
+    holds d (element 0) and e (element 3).  The carry is
+    ((Excl(1) (+) WX[4]) (+) LX[2]) = ((a+b)+c), and d and e are folded in
+    one at a time: ((((a+b)+c)+d)+e)."""
+    E, C = scan_geometry(dtype)
+    w4 = C + 4 * 32 * E
+    spots = {"a": 3, "b": C + 2 * 32 * E + 5, "c": w4 + E + 1,
+             "d": w4 + 2 * E, "e": w4 + 2 * E + 3}
+    n = w4 + 3 * E + 9
+    _segmented_fingerprint_case(dtype, E, [0, 3, n], [1], spots, w4 + 2 * E + 3,
+                                "((((a+b)+c)+d)+e)", 8)
+
+
+@pytest.mark.parametrize("dtype", [F32, F64])
+def test_segscan_fingerprint_element_fold_in_lane_head(dtype):
+    """A head inside a lane: lane 1 of warp 1 holds junk, then the head a,
+    then b and c.  The lane's carry (warp 0 and lane 0 of warp 1, all
+    before the head) and the junk must vanish at a, and b and c fold in
+    one at a time: ((a+b)+c)."""
+    E, C = scan_geometry(dtype)
+    lane = 32 * E + E
+    spots = {"a": lane + 2, "b": lane + 4, "c": lane + 5}
+    n = lane + E + 3
+    _segmented_fingerprint_case(dtype, E, [0, lane + 2, n], [0, 32 * E + 1, lane],
+                                spots, lane + 5, "((a+b)+c)", 9)
+
+
+@pytest.mark.parametrize("dtype", [F32, F64])
 def test_scan_exclusive_is_shifted_inclusive_and_reverse(dtype):
     x = workloads.scan_input(n=100000, dtype=dtype)
     inc, tot = oracle.det_scan(x)
