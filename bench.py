@@ -35,6 +35,7 @@ L2_BYTES = 129 * 1024 * 1024
 # GB300's FP64 rate: 1.25 TFLOP/s nominal, an FMA counted as two operations,
 # i.e. 0.625 T adds/s -- two FP64 lanes per SM per clock on 152 SMs at 2,070 MHz.
 FP64_ADDS_PER_S = 152 * 2 * 2.07e9
+FP64_MEASURED = {}     # {"rate": adds/s from the add-only probe, measured once per run}
 BLOCK_THREADS = 0      # --block-threads: launch shape of the library calls (never changes the bits)
 N_OVERRIDE = 0         # --n: element count of the sum and scan workloads (smaller cases for profiler captures)
 
@@ -135,7 +136,8 @@ def build_workload(name, torch, det, dev):
 
     if (name.startswith("scan") or name.startswith("segscan")) and name != "scan_i32":
         seg = name.startswith("segscan")
-        restart = name == "segscan_restart"
+        restart = name.startswith("segscan_restart")
+        sflags = (1 if "excl" in name else 0) | (2 if "rev" in name else 0)
         n = N_OVERRIDE or (workloads.SCAN_SMALL_N if "small" in name else workloads.SCAN_N)
         x_np = workloads.scan_input(n=n, dtype=npdt)
         x = torch.from_numpy(x_np).to(dev)
@@ -148,15 +150,15 @@ def build_workload(name, torch, det, dev):
             off = torch.from_numpy(off_np).to(dev)
             ws = det.workspace(det.lib().det_segmented_scan_workspace_bytes(n, off.numel() - 1, code), dev)
 
-            sflags = det.SCAN_SEGMENT_RESTART if restart else 0
+            gflags = sflags | (det.SCAN_SEGMENT_RESTART if restart else 0)
 
             def step():
-                det.det_segmented_scan(x, off, y, flags=sflags, workspace=ws, block_threads=BLOCK_THREADS)
+                det.det_segmented_scan(x, off, y, flags=gflags, workspace=ws, block_threads=BLOCK_THREADS)
         else:
             ws = det.workspace(det.lib().det_scan_workspace_bytes(n, code), dev)
 
             def step():
-                det.det_scan(x, y, workspace=ws, block_threads=BLOCK_THREADS)
+                det.det_scan(x, y, flags=sflags, workspace=ws, block_threads=BLOCK_THREADS)
 
         def e2e_step():
             x.copy_(host_x, non_blocking=True)
@@ -168,9 +170,10 @@ def build_workload(name, torch, det, dev):
             m = min(n, 1 << 24)
             if seg:
                 o = workloads.segment_offsets(m)
-                reps, secs = _timed_oracle(lambda: oracle.det_segmented_scan(x_np[:m], o, 4 if restart else 0))
+                reps, secs = _timed_oracle(
+                    lambda: oracle.det_segmented_scan(x_np[:m], o, sflags | (4 if restart else 0)))
             else:
-                reps, secs = _timed_oracle(lambda: oracle.det_scan(x_np[:m]))
+                reps, secs = _timed_oracle(lambda: oracle.det_scan(x_np[:m], sflags))
             return m * reps, secs, f"{reps} x {'segmented ' if seg else ''}scan of the first {m} elements, 1 thread"
 
         kern = ("det_segmented_scan_restart" if restart else "det_segmented_scan") if seg else "det_scan"
@@ -179,7 +182,9 @@ def build_workload(name, torch, det, dev):
                     adds=(2 * n) if dt == "f64" else None,
                     dominant=kern,
                     dtype=dt, e2e_step=e2e_step, h2d=n * s, d2h=n * s, oracle_sample=oracle_sample,
-                    config={"workload": f"{kern} forward inclusive n={n} lognormal(0,1) {dt} seed 4{extra}",
+                    config={"workload": f"{kern} {('reverse' if sflags & 2 else 'forward')} "
+                                        f"{('exclusive' if sflags & 1 else 'inclusive')} n={n} lognormal(0,1) {dt} "
+                                        f"seed 4{extra}", "flags": sflags,
                             "n": n, "l2": "inputs and outputs larger than L2; L2 flushed between timed steps"})
 
     if name in ("scatter_sub", "scatter_min", "scatter_max"):
@@ -681,9 +686,16 @@ def traffic_for(kernel, workload):
         return None
 
 
-OPS = ["sum", "sum_f64", "sum_small", "scatter_f64", "scatter_bin0", "skew", "skew_f32", "scan", "scan_f64",
-       "scan_small", "segscan", "rows", "scatter_sub", "scatter_min", "scatter_max", "scan_i32", "slot_alloc",
-       "slot_alloc_multi", "scatter_vec3", "rows_ordered", "gather_grad", "segscan_restart"]
+# Every configuration of the hot path at each dtype it names (a workload name
+# ending in _f64 is the f64 arm, any other the f32 arm), then the next rows.
+OPS = ["sum", "sum_f64", "sum_small", "sum_small_f64",
+       "scatter", "scatter_f64", "scatter_bin0", "scatter_bin0_f64",
+       "skew", "skew_f64",
+       "scan", "scan_f64", "scan_excl", "scan_rev", "scan_rev_excl", "scan_rev_excl_f64",
+       "scan_small", "scan_small_f64", "segscan", "segscan_f64",
+       "rows", "rows_f64",
+       "scatter_sub", "scatter_min", "scatter_max", "scan_i32", "slot_alloc", "slot_alloc_multi", "scatter_vec3",
+       "rows_ordered", "gather_grad", "segscan_restart", "segscan_restart_f64"]
 
 
 def measure_op(name, torch, det, dev, flush, steps, runs, peak):
@@ -711,6 +723,8 @@ def measure_op(name, torch, det, dev, flush, steps, runs, peak):
     if wl.get("adds") and dom_ms:
         res["kernel_Gadd_s"] = wl["adds"] / (dom_ms * 1e-3) / 1e9
         res["kernel_frac_of_fp64_add_peak"] = wl["adds"] / (dom_ms * 1e-3) / FP64_ADDS_PER_S
+        if FP64_MEASURED.get("rate"):
+            res["kernel_frac_of_measured_fp64_add_rate"] = wl["adds"] / (dom_ms * 1e-3) / FP64_MEASURED["rate"]
     res["distinct_results_det"] = len({wl["det_once"]() for _ in range(runs)})
     if "base_once" in wl:
         for _ in range(2):
@@ -733,6 +747,22 @@ def measure_op(name, torch, det, dev, flush, steps, runs, peak):
     del wl
     torch.cuda.empty_cache()
     return res
+
+
+def measure_add_rate(torch, det, dev, dtype):
+    """The device's add rate in `dtype` (adds/s): the add-only probe launch,
+    timed with CUDA events on the current stream, best of 5."""
+    sink = torch.zeros(1, dtype=dtype, device=dev)
+    stream = torch.cuda.current_stream()
+    best = 0.0
+    for _ in range(6):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        adds = det.add_rate_probe(dtype, 4096, sink)
+        e1.record(stream)
+        e1.synchronize()
+        best = max(best, adds / (e0.elapsed_time(e1) * 1e-3))
+    return best
 
 
 def run_det(args, torch, rank, world):
@@ -788,8 +818,11 @@ def run_det(args, torch, rank, world):
         # the FP64 add rate, not HBM, bounds this kernel: report against it
         hbm = {k: roofline[k] for k in ("achieved", "peak", "unit", "frac", "peak_kind")}
         a = adds / (dom_ms * 1e-3) / 1e9
+        measured = measure_add_rate(torch, det, dev, torch.float64)
         roofline.update({"bound": "alu", "achieved": a, "peak": FP64_ADDS_PER_S / 1e9, "unit": "Gadd/s",
-                         "frac": a * 1e9 / FP64_ADDS_PER_S, "peak_kind": "nominal FP64 add rate",
+                         "frac": a * 1e9 / FP64_ADDS_PER_S,
+                         "peak_kind": "nominal FP64 add rate (1.25 TFLOP/s, FMA = 2: 152 SMs x 2 adds x 2.07 GHz)",
+                         "measured_peak": measured / 1e9, "frac_of_measured": a * 1e9 / measured,
                          "algo_adds_per_launch": adds, "hbm": hbm})
 
     # end to end through host buffers (pinned), same metric
@@ -810,12 +843,14 @@ def run_det(args, torch, rank, world):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         elems, secs, what = wl["oracle_sample"]()
-        cpu = {"value": elems / secs / 1e9, "unit": "Gelem/s", "cores": 1, "kind": "oracle",
-               "sample": what}
+        cpu = dict({"value": elems / secs / 1e9, "unit": "Gelem/s", "cores": 1, "kind": "oracle",
+                    "sample": what}, **host_cpu())
 
     dtype, config = wl["dtype"], dict(wl["config"], parallelism=f"replicas{world}")
     ops = {}
     if args.ops and rank == 0:
+        FP64_MEASURED["rate"] = measure_add_rate(torch, det, dev, torch.float64)
+        FP64_MEASURED["f32_rate"] = measure_add_rate(torch, det, dev, torch.float32)
         # the headline workload's own determinism count and baseline, then
         # every other workload of the hot path, measured the same way
         add_checks(args.workload, wl, torch, det, dev)
@@ -837,6 +872,9 @@ def run_det(args, torch, rank, world):
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
             "clocks": clk.summary(), "step_ms_min": min(times), "step_ms_median": statistics.median(times),
             "algo_gbs_per_step": step_bytes / (ms_per_step * 1e-3) / 1e9, "ops": ops}
+    if FP64_MEASURED:
+        line["add_rate_probe_Gadd_s"] = {"f64": FP64_MEASURED["rate"] / 1e9, "f32": FP64_MEASURED["f32_rate"] / 1e9,
+                                         "f64_nominal": FP64_ADDS_PER_S / 1e9}
     return line
 
 
@@ -844,8 +882,6 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     import oracle  # noqa: F401
-    wl = build_workload(args.workload, None, None, None) if False else None
-    _ = wl
     # The reference arm is the CPU oracle, timed as it stands on the host cores.
     name = args.workload
     t_all = []
@@ -862,8 +898,33 @@ def run_reference(args, rank, world):
             "value": v, "unit": "Gelem/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": secs * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": ref_dtype(name), "data": "synthetic", "config": {"workload": name, "sample": what},
-            "cpu_baseline": {"value": v, "unit": "Gelem/s", "cores": 1, "kind": "oracle", "sample": what},
+            "cpu_baseline": dict({"value": v, "unit": "Gelem/s", "cores": 1, "kind": "oracle", "sample": what},
+                                 **host_cpu()),
             "e2e": {"value": v, "unit": "Gelem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def host_cpu():
+    """The host the oracle ran on: logical CPU count and model name."""
+    info = {"nproc": os.cpu_count()}
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.split(":")[0].strip() == "Model name":
+                model = ln.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            for ln in open("/proc/cpuinfo"):
+                if ln.lower().startswith(("model name", "cpu part")):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    info["cpu_model"] = model
+    return info
 
 
 def ref_dtype(name):
@@ -899,10 +960,11 @@ def ref_sample(name):
         n = 1 << 22
         x = workloads.scan_input(n=n, dtype=npdt)
         t0 = time.perf_counter()
+        fl = (1 if "excl" in name else 0) | (2 if "rev" in name else 0)
         if name.startswith("segscan"):
-            oracle.det_segmented_scan(x, workloads.segment_offsets(n))
+            oracle.det_segmented_scan(x, workloads.segment_offsets(n), fl | (4 if "restart" in name else 0))
         else:
-            oracle.det_scan(x)
+            oracle.det_scan(x, fl)
         return n, time.perf_counter() - t0, f"{name} of {n} elements"
     raise SystemExit(f"unknown workload {name}")
 

@@ -32,6 +32,7 @@
 // has a time limit: on expiry the status word gets DET_ERR_LOOKBACK_TIMEOUT
 // and all later waits of the launch give up at once.
 #include "det_common.cuh"
+#include "../../include/det_test_hooks.h"
 
 #include <algorithm>
 
@@ -182,6 +183,7 @@ template <typename T> struct ScanArgs {
   unsigned int* status;
   T* total_out;
   unsigned long long timeout_ns;
+  long long withhold;             // chunk whose aggregate is never published (test hook), else -1
 };
 
 // Shared memory of one CTA (dynamic): stage rows, then the small arrays.
@@ -379,7 +381,7 @@ __global__ void __launch_bounds__(1024, 1) scan_kernel(ScanArgs<T> a) {
     const bool aggf = __shfl_sync(0xffffffffu, (int)f, 31);
     if (lane == 0) {
       sm.wxf = wxm;
-      publish<T>(a.desc + c, agg);
+      if (c != a.withhold) publish<T>(a.desc + c, agg);
     }
     // look-back
     const long long k = c / 32;
@@ -590,7 +592,7 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
       if (lane == 0) {
         sm.wxf[set] = wxm;
         sm.wtf = 0u;   // read above; reset for the next phase 1
-        publish<T>(a.desc + c, agg);
+        if (c != a.withhold) publish<T>(a.desc + c, agg);
       }
     }
   };
@@ -1010,6 +1012,10 @@ __global__ void seg_heads_kernel(const long long* __restrict__ off, long long ns
 
 }  // namespace
 
+// Test hook state (det_test_hooks.h): host-side, read when a call is enqueued.
+static long long g_scan_withhold = -1;
+static unsigned long long g_scan_wait_ns = kWaitNs;
+
 template <typename T> struct ScanWs {
   size_t desc, anchors, tails, bits, has_head, total;
 };
@@ -1095,7 +1101,8 @@ static int scan_impl(const T* x, T* y, long long n, const long long* seg_off, lo
   a.role = &h->ticket2;
   a.status = &h->status;
   a.total_out = total_out;
-  a.timeout_ns = 2000000000ull;
+  a.timeout_ns = g_scan_wait_ns;
+  a.withhold = g_scan_withhold;
   const bool rev = flags & DET_SCAN_REVERSE, excl = flags & DET_SCAN_EXCLUSIVE;
   if (SEG) {
     if (cudaMemsetAsync(w + L.bits, 0, L.total - L.bits, s) != cudaSuccess) return DET_ERR_CUDA;
@@ -1201,4 +1208,16 @@ extern "C" int det_segmented_scan(const void* x, void* y, int64_t n, const int64
                                   flags, nullptr, workspace, workspace_bytes, block_threads, as_stream(stream));
   return scan_impl<double, true>((const double*)x, (double*)y, n, (const long long*)seg_offsets, num_segments,
                                  flags, nullptr, workspace, workspace_bytes, block_threads, as_stream(stream));
+}
+
+extern "C" int det_test_scan_withhold(int64_t chunk, uint64_t timeout_ns) {
+  if (chunk < 0) {
+    g_scan_withhold = -1;
+    g_scan_wait_ns = kWaitNs;
+    return DET_OK;
+  }
+  if (timeout_ns == 0 || timeout_ns > kWaitNs) return DET_ERR_INVALID_ARG;
+  g_scan_withhold = chunk;
+  g_scan_wait_ns = timeout_ns;
+  return DET_OK;
 }

@@ -61,6 +61,8 @@ _SIGNATURES = {
     "det_profile_event_count": (_int, []),
     "det_profile_event_name": (ctypes.c_char_p, [_int]),
     "det_launch_count": (ctypes.c_ulonglong, []),
+    "det_test_scan_withhold": (_int, [_i64, ctypes.c_uint64]),
+    "det_profile_add_rate_probe": (_int, [_int, _int, _vp, _vp, ctypes.POINTER(ctypes.c_ulonglong)]),
     "det_atomic_sum": (_int, [_vp, _i64, _int, _vp, _vp]),
     "det_atomic_scatter_add": (_int, [_vp, _i64, _vp, _vp, _i64, _int, _vp]),
     "det_atomic_scatter_add_rows": (_int, [_vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _int, _vp]),
@@ -414,6 +416,15 @@ class KernelTimer:
 
 def launch_count() -> int:
     return int(lib().det_launch_count())
+
+
+def add_rate_probe(dtype: torch.dtype, iters: int, sink: torch.Tensor, stream=None) -> int:
+    """Enqueue the add-only probe launch; returns the additions it performs."""
+    adds = ctypes.c_ulonglong(0)
+    code = F32 if dtype == torch.float32 else F64
+    _check(lib().det_profile_add_rate_probe(code, int(iters), _ptr(sink), _stream(stream), ctypes.byref(adds)),
+           "det_profile_add_rate_probe")
+    return int(adds.value)
 
 
 # ---------------------------------------------------------------------------

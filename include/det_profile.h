@@ -31,6 +31,19 @@ const char* det_profile_event_name(int i);
 /* Kernel launches made by this library since the process started. */
 unsigned long long det_launch_count(void);
 
+/* det_profile_add_rate_probe -- enqueue on `stream` one launch that only adds:
+ * every thread of (SMs x 8) CTAs of 256 threads runs 8 independent chains of
+ * `iters` dependent additions in `dtype` (DET_F32 or DET_F64), registers
+ * only.  Timed with CUDA events by the caller, *adds_out / time is the
+ * device's add rate for that type (the bound of the f64 sum and scan when
+ * FP64 arithmetic, not HBM, limits them).
+ *   sink      device, one element of dtype (never written in practice)
+ *   adds_out  host: the number of additions the launch performs
+ * Returns DET_OK, DET_ERR_DTYPE, DET_ERR_INVALID_ARG (iters <= 0, null
+ * pointer) or DET_ERR_CUDA. */
+int det_profile_add_rate_probe(int dtype, int iters, void* sink, void* stream,
+                               unsigned long long* adds_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -83,3 +83,9 @@ def test_host_checks_of_the_next_calls(lib):
     assert lib.det_scatter_sub(fake, 4, None, fake, 10, 0, None, None, fake, 1 << 20, 0, None) == 1
     assert lib.det_scan_i32_workspace_bytes(1 << 20) > 0 and lib.det_slot_alloc_workspace_bytes(1 << 20, 4) > 0
     assert lib.det_scatter_minmax_workspace_bytes(1000, 1) >= 8000
+
+
+def test_scan_withhold_hook_checks_its_limit(lib):
+    assert lib.det_test_scan_withhold(5, 0) == 1                 # no limit
+    assert lib.det_test_scan_withhold(5, 3 * 10**9) == 1         # above the 2 s default
+    assert lib.det_test_scan_withhold(-1, 0) == 0                # clearing always works
