@@ -76,15 +76,20 @@ __device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long lon
   return v;
 }
 
-// Publish a value word.  The all-ones pattern marks "not yet published"; the
-// only value with those bits is a NaN, which is published as the canonical
-// quiet NaN instead (NaN payloads are outside the bit-exact promise).
+// Published words hold the complement of the value's bits, so the all-zero
+// word -- what the call's one clearing memset leaves -- marks "not yet
+// published".  The only value whose complement is zero is the all-ones NaN,
+// which is published as the canonical quiet NaN instead (NaN payloads are
+// outside the bit-exact promise).
 template <typename T>
 __device__ __forceinline__ void publish(typename Bits<T>::U* p, T v) {
   typename Bits<T>::U b = to_bits<T>(v);
   if (b == Bits<T>::kSentinel) b = Bits<T>::kQNaN;
-  st_relaxed(p, b);
+  st_relaxed(p, ~b);
 }
+template <typename U> __device__ __forceinline__ bool is_published(U w) { return w != U(0); }
+__device__ __forceinline__ float decode(unsigned int w) { return from_bits(~w); }
+__device__ __forceinline__ double decode(unsigned long long w) { return from_bits(~w); }
 
 // Wait (bounded in time) for a published value word.  Returns false if the
 // launch has given up (this wait timed out, or another one did).
@@ -92,16 +97,16 @@ template <typename T>
 __device__ bool wait_value(const typename Bits<T>::U* p, T& out, unsigned int* status,
                            unsigned long long timeout_ns) {
   typename Bits<T>::U b = ld_relaxed(p);
-  if (b != Bits<T>::kSentinel) {
-    out = from_bits(b);
+  if (is_published(b)) {
+    out = decode(b);
     return true;
   }
   const unsigned long long t0 = globaltimer();
   unsigned int polls = 0;
   while (true) {
     b = ld_relaxed(p);
-    if (b != Bits<T>::kSentinel) {
-      out = from_bits(b);
+    if (is_published(b)) {
+      out = decode(b);
       return true;
     }
     if ((++polls & 63u) == 0) {
@@ -219,14 +224,14 @@ __device__ void anchor_chain(const ScanArgs<T>& a) {
     U b[kAhead];
 #pragma unroll
     for (int q = 0; q < kAhead; ++q)
-      b[q] = (kb + q < nint) ? ld_relaxed(a.desc + 32 * (kb + q) + lane) : Bits<T>::kSentinel;
+      b[q] = (kb + q < nint) ? ld_relaxed(a.desc + 32 * (kb + q) + lane) : U(0);
 #pragma unroll
     for (int q = 0; q < kAhead; ++q) {
       const long long k = kb + q;
       if (k >= nint) break;
       T mine;
-      if (b[q] != Bits<T>::kSentinel)
-        mine = from_bits(b[q]);
+      if (is_published(b[q]))
+        mine = decode(b[q]);
       else
         wait_value<T>(a.desc + 32 * k + lane, mine, a.status, a.timeout_ns);
       const bool minef = SEG && a.has_head[32 * k + lane];
@@ -1080,12 +1085,14 @@ static int scan_impl(const T* x, T* y, long long n, const long long* seg_off, lo
   const ScanWs<T> L = scan_ws_layout<T>(n, SEG);
   if (ws_bytes < L.total) return DET_ERR_WORKSPACE;
   char* w = reinterpret_cast<char*>(ws);
-  if (cudaMemsetAsync(w, 0, kHeaderBytes, s) != cudaSuccess) return DET_ERR_CUDA;
   if (n == 0) {
+    if (cudaMemsetAsync(w, 0, kHeaderBytes, s) != cudaSuccess) return DET_ERR_CUDA;
     if (total_out && cudaMemsetAsync(total_out, 0, sizeof(T), s) != cudaSuccess) return DET_ERR_CUDA;
     return DET_OK;
   }
-  if (cudaMemsetAsync(w + L.desc, 0xff, L.bits - L.desc, s) != cudaSuccess) return DET_ERR_CUDA;
+  // one clearing memset: the header, every published word ("unpublished"
+  // is all-zero) and, for segmented scans, the head bitmap and chunk flags
+  if (cudaMemsetAsync(w, 0, SEG ? L.total : L.bits, s) != cudaSuccess) return DET_ERR_CUDA;
   WsHeader* h = reinterpret_cast<WsHeader*>(ws);
   ScanArgs<T> a;
   a.x = x;
@@ -1105,7 +1112,6 @@ static int scan_impl(const T* x, T* y, long long n, const long long* seg_off, lo
   a.withhold = g_scan_withhold;
   const bool rev = flags & DET_SCAN_REVERSE, excl = flags & DET_SCAN_EXCLUSIVE;
   if (SEG) {
-    if (cudaMemsetAsync(w + L.bits, 0, L.total - L.bits, s) != cudaSuccess) return DET_ERR_CUDA;
     unsigned int* bits = reinterpret_cast<unsigned int*>(w + L.bits);
     unsigned char* hh = reinterpret_cast<unsigned char*>(w + L.has_head);
     a.head_bits = bits;

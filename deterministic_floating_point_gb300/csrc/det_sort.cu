@@ -797,20 +797,22 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
 
 // One CTA of 256 threads per rank-aligned 4096-record block of a long bin.
 // All leaves are read in one coalesced round (16 loads per thread in
-// flight) into shared memory; thread t then takes leaves [8t, 8t+8) of each
-// 2048-record half (a level-3 node), the warp's butterfly gives the level-8
-// node, the tree over the 8 warps the level-11 node and the two halves the
-// level-12 node -- the same node as any other aligned decomposition of the
-// block.  A second launch forms the PT over each bin's block nodes and adds
-// it to out[bin].
+// flight) into shared memory; thread t then reduces leaves [16t, 16t+16) in
+// registers (a level-4 node), and warp 0 takes the 256 thread nodes eight
+// per lane (level-7 nodes) and finishes with the shuffle levels (the
+// level-12 node) -- the same node as any other aligned decomposition of the
+// block.  Only the last eight levels run in one warp, so nearly every add
+// the SM issues is one of the tree's own (GB300's FP64 rate counts whole
+// warp instructions).  A second launch forms the PT over each bin's block
+// nodes and adds it to out[bin].
 template <typename T, bool NEG>
 __global__ void __launch_bounds__(256, sizeof(T) == 8 ? 5 : 8)
 segtree_blocks_kernel(const T* __restrict__ vals, const BlockDesc* __restrict__ blocks,
                       const unsigned int* __restrict__ nblocks, T* __restrict__ nodes, long long max_blocks,
                       long long max_lsegs) {
-  static_assert(kSegBlock == 2 * 256 * 8, "one CTA of 256 threads x 8 leaves per half block");
+  static_assert(kSegBlock == 256 * 16, "one CTA of 256 threads x 16 leaves");
   __shared__ __align__(16) T buf[kSegBlock];
-  __shared__ T wnode[2][8];
+  __shared__ T tnode[8 * 33];   // thread t's node at (t % 8) * 33 + t / 8: warp 0 reads it conflict-free
   const long long q = blockIdx.x;
   if (q >= (long long)*nblocks || q >= max_blocks) return;
   const int tid = threadIdx.x;
@@ -818,7 +820,7 @@ segtree_blocks_kernel(const T* __restrict__ vals, const BlockDesc* __restrict__ 
   if (B.sidx >= max_lsegs) return;
   const long long lo = B.lo, len = min((long long)kSegBlock, (long long)B.len);
   // leaves sit in shared memory with the 16-byte chunks of each 128-byte
-  // line XOR-permuted by the line index, so that the per-thread reads of 8
+  // line XOR-permuted by the line index, so that the per-thread reads of 16
   // consecutive leaves are conflict-free
   constexpr int EPC = 16 / (int)sizeof(T);   // leaves per 16-byte chunk
   auto pchunk = [](int c) { return c ^ ((c >> 3) & 7); };
@@ -828,28 +830,23 @@ segtree_blocks_kernel(const T* __restrict__ vals, const BlockDesc* __restrict__ 
     buf[pchunk(j / EPC) * EPC + j % EPC] = j < len ? (NEG ? -__ldg(vals + lo + j) : __ldg(vals + lo + j)) : absent<T>();
   }
   __syncthreads();
-  constexpr int NQ = 8 * (int)sizeof(T) / 16;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  {
+    constexpr int NQ = 16 * (int)sizeof(T) / 16;
     float4 q4[NQ];
-    const int c0 = (h * (kSegBlock / 2) + tid * 8) / EPC;
+    const int c0 = tid * 16 / EPC;
 #pragma unroll
     for (int i = 0; i < NQ; ++i) q4[i] = reinterpret_cast<const float4*>(buf)[pchunk(c0 + i)];
-    T v[8];
+    T v[16];
     memcpy(v, q4, sizeof(v));
-    const T node = warp_pt(thread_pt(v));
-    if ((tid & 31) == 0) wnode[h][tid >> 5] = node;
+    tnode[(tid & 7) * 33 + (tid >> 3)] = thread_pt(v);
   }
   __syncthreads();
-  if (tid == 0) {
-    T half[2];
+  if (tid < 32) {
+    T v[8];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const T a01 = wnode[h][0] + wnode[h][1], a23 = wnode[h][2] + wnode[h][3];
-      const T a45 = wnode[h][4] + wnode[h][5], a67 = wnode[h][6] + wnode[h][7];
-      half[h] = (a01 + a23) + (a45 + a67);
-    }
-    nodes[q] = half[0] + half[1];
+    for (int i = 0; i < 8; ++i) v[i] = tnode[i * 33 + tid];   // thread node 8 * tid + i
+    const T node = warp_pt(thread_pt(v));
+    if (tid == 0) nodes[q] = node;
   }
 }
 

@@ -14,8 +14,12 @@
 //   warp-block 32 lanes = 4 KB, five xor-shuffle levels      -> level 10 / 9
 //   tile       2^tb warp-blocks per CTA (host-chosen power of two), nodes
 //              staged in shared memory and reduced by PT
-//   final      the last CTA to finish (integer ticket) reduces the tile
-//              partials by PT and writes the scalar.
+//   final      PT over the tile partials, by one CTA.  det_sum: the last
+//              CTA of the grid waits for every tile's flag, tagged with this
+//              call's generation number, so nothing is cleared between calls
+//              and a call is one launch.  det_sum_noalloc: the last CTA to
+//              finish, by an integer ticket cleared before the launch.
+#include <atomic>
 #include <mutex>
 
 #include "det_common.cuh"
@@ -24,10 +28,41 @@ namespace det {
 namespace {
 
 template <typename T> struct SumGeom {
-  static constexpr int LE = 128 / sizeof(T);   // elements per lane
+  static constexpr int CE = 128 / sizeof(T);   // elements per 128-byte lane chunk
+  static constexpr int LE = sizeof(T) == 4 ? 32 : 64;   // elements per lane
   static constexpr int WB = kWarp * LE;        // elements per warp-block
   static constexpr int V = Vec256<T>::N;       // elements per 256-bit load
 };
+
+// The lane's node over LE contiguous elements at p (absent past n): PT of
+// each 128-byte chunk in registers, then PT over the chunk nodes.  For f64 a
+// lane takes four chunks, so that only one add in sixteen runs at the
+// warp-shuffle levels, where every lane of the warp issues it.
+template <typename T, bool VEC>
+__device__ __forceinline__ T lane_node(const T* __restrict__ x, long long base, long long n) {
+  using G = SumGeom<T>;
+  constexpr int NC = G::LE / G::CE;
+  T cn[NC];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const long long cb = base + c * G::CE;
+    T v[G::CE];
+    if (VEC && cb + G::CE <= n) {
+#pragma unroll
+      for (int q = 0; q < G::CE / G::V; ++q) {
+        T w[G::V];
+        ld_nc_256(x + cb + q * G::V, w);
+#pragma unroll
+        for (int e = 0; e < G::V; ++e) v[q * G::V + e] = w[e];
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < G::CE; ++e) v[e] = (cb + e < n) ? x[cb + e] : absent<T>();
+    }
+    cn[c] = thread_pt(v);
+  }
+  return thread_pt(cn);
+}
 
 // PT over p[0..L) by a whole CTA; the result is returned to thread 0.
 // Thread t reduces the aligned group [t g, (t+1) g) with g = max(1, P / T)
@@ -73,10 +108,17 @@ __device__ T cta_pt_global(const T* p, long long L, T* smem_warp) {
   return r;
 }
 
-template <typename T, bool VEC>
+// FLAGS: tile t publishes flags[t] = gen after its partial; the grid's last
+// CTA waits (bounded in time) for every flag, then forms the final tree and
+// writes the status word itself.  CTAs start in index order, so when the
+// last one runs every other tile has started and only needs to finish; the
+// flags of earlier calls carry other generation numbers, so nothing needs
+// clearing between calls.
+template <typename T, bool VEC, bool FLAGS>
 __global__ void __launch_bounds__(1024)
 sum_kernel(const T* __restrict__ x, long long n, int tb_log2, long long ntiles, T* __restrict__ partials,
-           unsigned int* __restrict__ ticket, T* __restrict__ out) {
+           unsigned int* __restrict__ ticket, T* __restrict__ out, unsigned long long* __restrict__ flags,
+           unsigned long long gen, unsigned int* __restrict__ status) {
   using G = SumGeom<T>;
   __shared__ T nodes[1024];
   __shared__ T warp_nodes[32];
@@ -87,20 +129,7 @@ sum_kernel(const T* __restrict__ x, long long n, int tb_log2, long long ntiles, 
 
   for (int b = warp; b < TB; b += nwarps) {
     const long long base = tile_base + (long long)b * G::WB + (long long)lane * G::LE;
-    T v[G::LE];
-    if (VEC && base + G::LE <= n) {
-#pragma unroll
-      for (int q = 0; q < G::LE / G::V; ++q) {
-        T w[G::V];
-        ld_nc_256(x + base + q * G::V, w);
-#pragma unroll
-        for (int e = 0; e < G::V; ++e) v[q * G::V + e] = w[e];
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < G::LE; ++e) v[e] = (base + e < n) ? x[base + e] : absent<T>();
-    }
-    T node = warp_pt(thread_pt(v));
+    T node = warp_pt(lane_node<T, VEC>(x, base, n));
     if (lane == 0) nodes[b] = node;
   }
   __syncthreads();
@@ -122,13 +151,35 @@ sum_kernel(const T* __restrict__ x, long long n, int tb_log2, long long ntiles, 
     node = warp_pt(node);
     if (lane == 0) {
       partials[blockIdx.x] = node;
-      __threadfence();
-      unsigned int t = atomicAdd(ticket, 1u);
-      is_last = (t == (unsigned int)(ntiles - 1));
+      if (FLAGS) {
+        st_release_u64(flags + blockIdx.x, gen);   // orders the partial before the flag
+        is_last = blockIdx.x == ntiles - 1;
+      } else {
+        __threadfence();
+        unsigned int t = atomicAdd(ticket, 1u);
+        is_last = (t == (unsigned int)(ntiles - 1));
+      }
     }
   }
   __syncthreads();
   if (!is_last) return;
+  if (FLAGS) {
+    // every tile's flag carries this call's generation (bounded wait)
+    bool ok = true;
+    const unsigned long long t0 = globaltimer();
+    for (long long t = threadIdx.x; t < ntiles && ok; t += blockDim.x) {
+      unsigned polls = 0;
+      while (ld_acquire_u64(flags + t) != gen) {
+        if ((++polls & 63u) == 0 && globaltimer() - t0 > kWaitNs) {
+          ok = false;
+          break;
+        }
+      }
+    }
+    ok = __syncthreads_and(ok);
+    if (threadIdx.x == 0) *status = ok ? (unsigned)DET_OK : (unsigned)DET_ERR_LOOKBACK_TIMEOUT;
+    if (!ok) return;
+  }
   __threadfence();
   // Partials were written by other CTAs: read them through L2 (volatile).
   T r = cta_pt_global<T>((const T*)partials, ntiles, warp_nodes);
@@ -161,10 +212,15 @@ static long long sum_ntiles(long long n, int* tb_log2) {
 
 using namespace det;
 
+// Per-call generation numbers of the single-launch path: unique within the
+// process, never 0 (a zeroed flag never matches).
+static std::atomic<unsigned long long> g_sum_gen{0};
+
+// Workspace: header, tile partials, tile flags (one 8-byte word per tile).
 extern "C" size_t det_sum_workspace_bytes(int64_t n, int dtype) {
   if (n < 0 || !valid_dtype(dtype)) return 0;
   long long nt = dtype == DET_F32 ? sum_ntiles<float>(n, nullptr) : sum_ntiles<double>(n, nullptr);
-  return kHeaderBytes + align_up((size_t)nt * elem_size(dtype), 256);
+  return kHeaderBytes + align_up((size_t)nt * elem_size(dtype), 256) + align_up((size_t)nt * 8, 256);
 }
 
 template <typename T>
@@ -174,19 +230,26 @@ static int det_sum_impl(const T* x, long long n, T* out, void* ws, size_t ws_byt
   long long nt = sum_ntiles<T>(n, &tb);
   if (ws_bytes < det_sum_workspace_bytes(n, sizeof(T) == 4 ? DET_F32 : DET_F64)) return DET_ERR_WORKSPACE;
   WsHeader* h = reinterpret_cast<WsHeader*>(ws);
-  if (cudaMemsetAsync(h, 0, kHeaderBytes, s) != cudaSuccess) return DET_ERR_CUDA;
   if (n == 0) {
+    if (cudaMemsetAsync(h, 0, kHeaderBytes, s) != cudaSuccess) return DET_ERR_CUDA;
     if (cudaMemsetAsync(out, 0, sizeof(T), s) != cudaSuccess) return DET_ERR_CUDA;
     return DET_OK;
   }
   T* partials = reinterpret_cast<T*>(reinterpret_cast<char*>(ws) + kHeaderBytes);
+  unsigned long long* flags = reinterpret_cast<unsigned long long*>(
+      reinterpret_cast<char*>(ws) + kHeaderBytes + align_up((size_t)nt * sizeof(T), 256));
   const int threads = bt ? bt : (tb >= 3 ? 256 : 32 << tb);
   const bool vec = (reinterpret_cast<uintptr_t>(x) % 32) == 0;
+  // one launch: the grid's last CTA forms the final tree once every tile's
+  // flag carries this call's generation number
+  const unsigned long long gen = ++g_sum_gen;
   launch_begin("det_sum", s);
   if (vec)
-    sum_kernel<T, true><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out);
+    sum_kernel<T, true, true><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out, flags, gen,
+                                                                &h->status);
   else
-    sum_kernel<T, false><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out);
+    sum_kernel<T, false, true><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out, flags, gen,
+                                                                 &h->status);
   launch_end(s);
   return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
 }
@@ -251,9 +314,11 @@ int det_sum_noalloc_impl(const T* x, long long n, T* out, int bt, cudaStream_t s
   const bool vec = (reinterpret_cast<uintptr_t>(x) % 32) == 0;
   launch_begin("det_sum_noalloc", s);
   if (vec)
-    sum_kernel<T, true><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out);
+    sum_kernel<T, true, false><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out, nullptr,
+                                                                 0ull, nullptr);
   else
-    sum_kernel<T, false><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out);
+    sum_kernel<T, false, false><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out, nullptr,
+                                                                  0ull, nullptr);
   launch_end(s);
   return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
 }
