@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/det.h"
 
 namespace det {
@@ -260,6 +262,14 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned pari
   return true;
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_dep() may be
+// launched while the previous kernel of the stream is still running; it
+// calls dep_wait() before any global memory access, which returns once that
+// kernel has completed and its writes are visible.  What overlaps is the
+// launch itself (the CTAs are already resident when the wait returns), not
+// the work.  For a kernel launched the ordinary way dep_wait() is a no-op.
+__device__ __forceinline__ void dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Host-side helpers -----------------------------------------------------------
 inline bool valid_block_threads(int bt) {
   return bt == 0 || bt == 128 || bt == 256 || bt == 512 || bt == 1024;
@@ -282,5 +292,24 @@ int kernel_occupancy(const void* kernel, int threads, size_t smem);
 // kernel launch of the library goes through launch_begin / launch_end.
 void launch_begin(const char* name, cudaStream_t s);
 void launch_end(cudaStream_t s);
+
+// Launch `kernel` with programmatic stream serialization: it may be launched
+// before the previous kernel in the stream completes, and waits for it in
+// dep_wait().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dep(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace det

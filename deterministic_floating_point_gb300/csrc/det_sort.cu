@@ -59,6 +59,7 @@ struct PassArgs {
 // test.  The first pass takes the lowest digit, so it never shifts.
 template <bool FIRST, bool OFFSET>
 __global__ void __launch_bounds__(256) sort_count_kernel(PassArgs a, long long K) {
+  dep_wait();   // launched early (programmatic dependent launch): wait for the previous kernel
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ __align__(8) unsigned long long keys_bar;
   const int ndig = 1 << a.D;
@@ -125,6 +126,7 @@ __global__ void __launch_bounds__(256) sort_count_kernel(PassArgs a, long long K
 // warp reads 8 consecutive digits of 4 tiles: whole 32-byte sectors).
 constexpr int kColDigits = 8, kColGroups = 128;
 __global__ void __launch_bounds__(1024) sort_colscan_kernel(PassArgs a, int count_valid) {
+  dep_wait();   // launched early (programmatic dependent launch): wait for the previous kernel
   __shared__ unsigned int part[kColGroups][kColDigits + 1];
   const int dl = threadIdx.x % kColDigits, g = threadIdx.x / kColDigits;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -425,6 +427,7 @@ __device__ __forceinline__ void rank_subpass(unsigned (&rec)[kIPT], unsigned* __
 // component's groups come out contiguous for the segmented tree.
 template <int VB, bool FIRST, bool IDX, bool KEYS_OUT, bool WIDE = false>
 __global__ void __launch_bounds__(512, 2) sort_pass_kernel(PassArgs a) {
+  dep_wait();   // launched early (programmatic dependent launch): wait for the previous kernel
   using U = typename Payload<VB>::U;
   constexpr bool IDX_IN = IDX && !FIRST;                // input indices carried from the previous pass
   constexpr bool RANK = VB == 0 && !IDX && !KEYS_OUT;   // only each record's sorted position is wanted
@@ -620,6 +623,7 @@ __global__ void __launch_bounds__(512, 2) sort_pass_kernel(PassArgs a) {
 template <int kBoundsPer>
 __global__ void sort_bounds_kernel(const int32_t* __restrict__ keys, const unsigned int* __restrict__ n_valid,
                                    long long m, int32_t* __restrict__ seg, long long n) {
+  dep_wait();   // launched early (programmatic dependent launch): wait for the previous kernel
   const long long i0 = kBoundsPer * ((long long)blockIdx.x * blockDim.x + threadIdx.x);
   const long long N = min((long long)*n_valid, n);
   if (i0 > N) return;
@@ -726,6 +730,7 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
                     unsigned int* __restrict__ nblocks, unsigned int* __restrict__ nlsegs,
                     const unsigned int* __restrict__ n_valid, long long max_blocks, long long max_lsegs,
                     unsigned int* __restrict__ status, long long ostride) {
+  dep_wait();   // launched early (programmatic dependent launch): wait for the previous kernel
   const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int lane = threadIdx.x & 31;
   const long long N = *n_valid;
@@ -795,8 +800,9 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
   }
 }
 
-// One CTA of 256 threads per rank-aligned 4096-record block of a long bin.
-// All leaves are read in one coalesced round (16 loads per thread in
+// A CTA of 256 threads per rank-aligned 4096-record block of a long bin, a
+// block at a time (persistent CTAs: the largest possible block count is far
+// above the real one, which only the device knows).  All leaves are read in one coalesced round (16 loads per thread in
 // flight) into shared memory; thread t then reduces leaves [16t, 16t+16) in
 // registers (a level-4 node), and warp 0 takes the 256 thread nodes eight
 // per lane (level-7 nodes) and finishes with the shuffle levels (the
@@ -806,19 +812,24 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
 // warp instructions).  A second launch forms the PT over each bin's block
 // nodes and adds it to out[bin].
 template <typename T, bool NEG>
-__global__ void __launch_bounds__(256, sizeof(T) == 8 ? 5 : 8)
+__global__ void __launch_bounds__(256, sizeof(T) == 8 ? 5 : 6)
 segtree_blocks_kernel(const T* __restrict__ vals, const BlockDesc* __restrict__ blocks,
                       const unsigned int* __restrict__ nblocks, T* __restrict__ nodes, long long max_blocks,
                       long long max_lsegs) {
+  dep_wait();   // launched early (programmatic dependent launch): wait for the previous kernel
   static_assert(kSegBlock == 256 * 16, "one CTA of 256 threads x 16 leaves");
   __shared__ __align__(16) T buf[kSegBlock];
   __shared__ T tnode[8 * 33];   // thread t's node at (t % 8) * 33 + t / 8: warp 0 reads it conflict-free
-  const long long q = blockIdx.x;
-  if (q >= (long long)*nblocks || q >= max_blocks) return;
   const int tid = threadIdx.x;
+  // block counts and record positions are below 2^31 (sort sizes are)
+  const unsigned nb = (unsigned)min((long long)*nblocks, max_blocks);
+  // persistent: the launch is sized by the SMs, not by the largest possible
+  // block count (only known on the device)
+  for (unsigned q = blockIdx.x; q < nb; q += gridDim.x) {
   const BlockDesc B = blocks[q];
-  if (B.sidx >= max_lsegs) return;
-  const long long lo = B.lo, len = min((long long)kSegBlock, (long long)B.len);
+  if (B.sidx >= max_lsegs) continue;
+  const T* __restrict__ leaves = vals + B.lo;
+  const int len = (int)min((unsigned)kSegBlock, B.len);
   // leaves sit in shared memory with the 16-byte chunks of each 128-byte
   // line XOR-permuted by the line index, so that the per-thread reads of 16
   // consecutive leaves are conflict-free
@@ -827,7 +838,7 @@ segtree_blocks_kernel(const T* __restrict__ vals, const BlockDesc* __restrict__ 
 #pragma unroll
   for (int i = 0; i < kSegBlock / 256; ++i) {
     const int j = i * 256 + tid;
-    buf[pchunk(j / EPC) * EPC + j % EPC] = j < len ? (NEG ? -__ldg(vals + lo + j) : __ldg(vals + lo + j)) : absent<T>();
+    buf[pchunk(j / EPC) * EPC + j % EPC] = j < len ? (NEG ? -__ldg(leaves + j) : __ldg(leaves + j)) : absent<T>();
   }
   __syncthreads();
   {
@@ -848,6 +859,8 @@ segtree_blocks_kernel(const T* __restrict__ vals, const BlockDesc* __restrict__ 
     const T node = warp_pt(thread_pt(v));
     if (tid == 0) nodes[q] = node;
   }
+  __syncthreads();   // buf and tnode are reused by the next block
+  }
 }
 
 // One warp per long bin: the PT over the bin's block nodes (in block order,
@@ -857,11 +870,14 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 segtree_finish_kernel(const LongSeg* __restrict__ lsegs, const unsigned int* __restrict__ nlsegs,
                       const T* __restrict__ nodes, T* __restrict__ out, long long max_lsegs, long long ostride) {
-  const long long sidx = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (sidx >= min((long long)*nlsegs, max_lsegs)) return;
-  const LongSeg L = lsegs[sidx];
-  const T t = warp_pt_range<T>(nodes + L.base, L.nblk);   // nodes already hold the negated leaves
-  if ((threadIdx.x & 31) == 0) out[L.bin * ostride] = out[L.bin * ostride] + t;
+  dep_wait();   // launched early (programmatic dependent launch): wait for the previous kernel
+  const long long ns = min((long long)*nlsegs, max_lsegs);
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long sidx = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; sidx < ns; sidx += nwarps) {
+    const LongSeg L = lsegs[sidx];
+    const T t = warp_pt_range<T>(nodes + L.base, L.nblk);   // nodes already hold the negated leaves
+    if ((threadIdx.x & 31) == 0) out[L.bin * ostride] = out[L.bin * ostride] + t;
+  }
 }
 
 }  // namespace
@@ -958,9 +974,9 @@ static cudaError_t launch_pass(const PassArgs& a, bool first, bool idx, bool key
   cudaError_t e = ensure_dyn_smem((const void*)k, smem);
   if (e != cudaSuccess) return e;
   launch_begin("det_sort_pass", s);
-  k<<<(unsigned)tiles, threads, smem, s>>>(a);
+  const cudaError_t le = launch_dep(k, dim3((unsigned)tiles), dim3(threads), smem, s, a);
   launch_end(s);
-  return cudaGetLastError();
+  return le;
 }
 
 int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key_offset, const void* values,
@@ -1015,13 +1031,14 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
     const cudaError_t ce = ensure_dyn_smem((const void*)ck, csmem);
     if (ce != cudaSuccess) return cuda_fail(ce, "sort: digit counts");
     launch_begin("det_sort_count", s);
-    ck<<<(unsigned)p.tiles, 256, csmem, s>>>(a, K);
+    const cudaError_t e1 = launch_dep(ck, dim3((unsigned)p.tiles), dim3(256), csmem, s, a, K);
     launch_end(s);
+    if (e1 != cudaSuccess) return cuda_fail(e1, "sort: digit counts");
     launch_begin("det_sort_colscan", s);
-    sort_colscan_kernel<<<(unsigned)((ndig + kColDigits - 1) / kColDigits), 1024, 0, s>>>(a, first ? 1 : 0);
+    const cudaError_t e2 = launch_dep(sort_colscan_kernel, dim3((unsigned)((ndig + kColDigits - 1) / kColDigits)),
+                                      dim3(1024), 0, s, a, first ? 1 : 0);
     launch_end(s);
-    const int rc = check_launch("sort: digit counts");
-    if (rc != DET_OK) return rc;
+    if (e2 != cudaSuccess) return cuda_fail(e2, "sort: column scan");
     const bool keys_out = p.passes > 1;
     cudaError_t e;
     if (p.wide)
@@ -1038,13 +1055,17 @@ int enqueue_sort(const SortPlan& p, void* ws, const int32_t* keys, long long key
   if (p.passes > 1) {   // one-pass sorts got their segment starts from the pass
     launch_begin("det_sort_bounds", s);
     const int32_t* fkeys = reinterpret_cast<const int32_t*>(w + p.keys[*final_buf]);
-    if (p.n > (1LL << 24))
-      sort_bounds_kernel<16><<<(unsigned)((p.n + 1 + 4095) / 4096), 256, 0, s>>>(fkeys, &h->n_valid, p.m, seg, p.n);
-    else
-      sort_bounds_kernel<4><<<(unsigned)((p.n + 1 + 1023) / 1024), 256, 0, s>>>(fkeys, &h->n_valid, p.m, seg, p.n);
+    const unsigned int* nv = &h->n_valid;
+    const cudaError_t e3 =
+        p.n > (1LL << 24)
+            ? launch_dep(sort_bounds_kernel<16>, dim3((unsigned)((p.n + 1 + 4095) / 4096)), dim3(256), 0, s, fkeys, nv,
+                         p.m, seg, p.n)
+            : launch_dep(sort_bounds_kernel<4>, dim3((unsigned)((p.n + 1 + 1023) / 1024)), dim3(256), 0, s, fkeys, nv,
+                         p.m, seg, p.n);
     launch_end(s);
+    if (e3 != cudaSuccess) return cuda_fail(e3, "sort: segment starts");
   }
-  return check_launch("sort: segment starts");
+  return DET_OK;
 }
 
 template <typename T>
@@ -1061,24 +1082,27 @@ int enqueue_segmented_tree(const SortPlan& p, void* ws, const T* sorted_vals, T*
     return DET_ERR_CUDA;
   launch_begin("det_segtree_bins", s);
   auto* kb = negate ? segtree_bins_kernel<T, true> : segtree_bins_kernel<T, false>;
-  kb<<<(unsigned)((p.m + 255) / 256), 256, 0, s>>>(sorted_vals, seg, p.m, out, blocks, lsegs,
-                                                         &h->long_blocks, &h->long_segs, &h->n_valid, p.max_blocks,
-                                                         p.max_lsegs, &h->status, ostride);
+  const cudaError_t eb =
+      launch_dep(kb, dim3((unsigned)((p.m + 255) / 256)), dim3(256), 0, s, sorted_vals, seg, p.m, out, blocks, lsegs,
+                 &h->long_blocks, &h->long_segs, (const unsigned int*)&h->n_valid, p.max_blocks, p.max_lsegs,
+                 &h->status, ostride);
   launch_end(s);
-  const int rc = check_launch("segmented tree: bins");
-  if (rc != DET_OK) return rc;
+  if (eb != cudaSuccess) return cuda_fail(eb, "segmented tree: bins");
   launch_begin("det_segtree_blocks", s);
   auto* kk = negate ? segtree_blocks_kernel<T, true> : segtree_blocks_kernel<T, false>;
-  kk<<<(unsigned)p.max_blocks, 256, 0, s>>>(sorted_vals, blocks, &h->long_blocks, nodes, p.max_blocks,
-                                            p.max_lsegs);
+  const long long sms = std::max(device_sm_count(), 1);
+  const cudaError_t ek = launch_dep(kk, dim3((unsigned)std::min(p.max_blocks, sms * 32)), dim3(256), 0, s,
+                                    sorted_vals, (const BlockDesc*)blocks, (const unsigned int*)&h->long_blocks,
+                                    nodes, p.max_blocks, p.max_lsegs);
   launch_end(s);
-  const int rc2 = check_launch("segmented tree: blocks");
-  if (rc2 != DET_OK) return rc2;
+  if (ek != cudaSuccess) return cuda_fail(ek, "segmented tree: blocks");
   launch_begin("det_segtree_finish", s);
-  segtree_finish_kernel<T><<<(unsigned)((p.max_lsegs * 32 + 255) / 256), 256, 0, s>>>(lsegs, &h->long_segs, nodes, out,
-                                                                                    p.max_lsegs, ostride);
+  const cudaError_t ef =
+      launch_dep(segtree_finish_kernel<T>, dim3((unsigned)std::min((p.max_lsegs * 32 + 255) / 256, sms * 32)),
+                 dim3(256), 0, s, (const LongSeg*)lsegs, (const unsigned int*)&h->long_segs, (const T*)nodes, out,
+                 p.max_lsegs, ostride);
   launch_end(s);
-  return check_launch("segmented tree: finish");
+  return ef == cudaSuccess ? DET_OK : cuda_fail(ef, "segmented tree: finish");
 }
 
 template int enqueue_segmented_tree<float>(const SortPlan&, void*, const float*, float*, cudaStream_t, bool, long long,
