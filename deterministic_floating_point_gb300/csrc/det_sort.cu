@@ -740,12 +740,37 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
     lo = max(0LL, min((long long)seg[b], hi));
     len = hi - lo;
   }
-  if (len > 0 && len <= kMediumGroup) {
+  // groups of at most one 128-byte chunk: PT over the group padded to W, the
+  // warp's largest such group rounded up to a power of two (padding beyond
+  // the group is absent, so any W >= len gives the same bits; a small W keeps
+  // warps of tiny groups from issuing adds on padding alone -- every FP64 add
+  // instruction costs the whole warp's width)
+  constexpr int CW = 128 / (int)sizeof(T);
+  const bool in_chunk = len > 0 && len <= CW;
+  const unsigned wmax = __reduce_max_sync(0xffffffffu, in_chunk ? (unsigned)len : 0u);
+  if (wmax > 0) {
+    T t = absent<T>();
+    const T* g = vals + lo;
+    const long long gl = in_chunk ? len : 0;
+    if (wmax <= 1)
+      t = thread_group_pt<T, NEG, 1>(g, gl);
+    else if (wmax <= 2)
+      t = thread_group_pt<T, NEG, 2>(g, gl);
+    else if (wmax <= 4)
+      t = thread_group_pt<T, NEG, 4>(g, gl);
+    else if (wmax <= 8)
+      t = thread_group_pt<T, NEG, 8>(g, gl);
+    else if (wmax <= 16)
+      t = thread_group_pt<T, NEG, 16>(g, gl);
+    else
+      t = thread_group_pt<T, NEG, CW>(g, gl);
+    if (in_chunk) out[b * ostride] = out[b * ostride] + t;
+  }
+  if (len > CW && len <= kMediumGroup) {
     // rank-aligned chunks of 128 bytes of leaves (level-5 nodes for f32,
     // level-4 for f64; absent terms past the group) merged by a binary
     // counter.  Neighbouring bins have similar sizes in practice, so the
     // lanes of a warp mostly run the same number of chunks.
-    constexpr int CW = 128 / (int)sizeof(T);
     NodeCounter<T, 6> nc;
     for (long long c = 0; c < len; c += CW) nc.push(thread_group_pt<T, NEG, CW>(vals + lo + c, len - c));
     out[b * ostride] = out[b * ostride] + nc.result();
