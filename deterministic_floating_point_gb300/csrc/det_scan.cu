@@ -173,6 +173,43 @@ __device__ __forceinline__ void regs_to_global_256(T* p, const T (&x)[E]) {
   }
 }
 
+// Store a warp's 32 lanes x E elements (each lane E consecutive elements of
+// y, the lanes' rows adjacent: the warp's span [ylo, ylo + 32 E) of y) with
+// coalesced 16-byte stores, through a 2 KB buffer of the warp: 16 lane rows
+// at a time, rows written with their 16-byte chunks XOR-swizzled by the row
+// (conflict-free), then read back as consecutive chunks.  REVERSED: the
+// lanes' rows and the elements inside a row are in descending address order.
+// ylo must be 16-byte aligned.
+template <typename T, int E, bool REVERSED>
+__device__ __forceinline__ void warp_store_staged(T* __restrict__ buf, const T (&x)[E], T* __restrict__ ylo,
+                                                  int lane) {
+  constexpr int P = 16 / (int)sizeof(T);   // elements per 16-byte chunk
+  constexpr int CH = E / P;                // chunks per lane row
+  static_assert(CH == 8, "a lane row is one 128-byte line");
+  const int pos = REVERSED ? 31 - lane : lane;   // the lane row's place in the span
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if ((pos >> 4) == h) {
+      const int r = pos & 15;
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        T v[P];
+#pragma unroll
+        for (int k = 0; k < P; ++k) v[k] = REVERSED ? x[E - 1 - (c * P + k)] : x[c * P + k];
+        *reinterpret_cast<float4*>(buf + (r * CH + (c ^ (r & 7))) * P) = *reinterpret_cast<const float4*>(v);
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 16 * CH / 32; ++k) {
+      const int i = lane + 32 * k, r = i / CH, c = i % CH;
+      const float4 v = *reinterpret_cast<const float4*>(buf + (r * CH + (c ^ (r & 7))) * P);
+      __stcs(reinterpret_cast<float4*>(ylo + (h * 16 + r) * E + c * P), v);
+    }
+    __syncwarp();
+  }
+}
+
 template <typename T> struct ScanArgs {
   const T* x;
   T* y;
@@ -510,6 +547,9 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   T* stage = reinterpret_cast<T*>(smem_raw);
   KeepSmem<T>& sm = *reinterpret_cast<KeepSmem<T>*>(smem_raw + G::kStageBytes);
+  // per-warp 2 KB output buffers (coalesced stores)
+  T* obuf = reinterpret_cast<T*>(smem_raw + G::kStageBytes + align_up(sizeof(KeepSmem<T>), 16)) +
+            (threadIdx.x >> 5) * (2048 / sizeof(T));
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int t0 = tid * E;   // first element of this thread's virtual lane (w = warp, l = lane)
 
@@ -778,15 +818,21 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
       T pl = __shfl_up_sync(0xffffffffu, x[E - 1], 1);
       __syncthreads();
       if (lane == 0) pl = (w > 0) ? sm.last[w - 1] : T(0.0);   // chunk start: written later
-#pragma unroll
       const unsigned hw = lane_heads(hb);
 #pragma unroll
       for (int e = E - 1; e > 0; --e) x[e] = (SEG && ((hw >> e) & 1u)) ? T(0.0) : x[e - 1];
       x[0] = (SEG && (hw & 1u)) ? T(0.0) : pl;
     }
     {
+      // forward f32 scans store through the warp's buffer (coalesced); the
+      // others lane by lane, a full 32-byte sector per store (measured faster
+      // for them: f64 scans are bound by the FP64 add rate)
+      constexpr bool kStaged = sizeof(T) == 4 && !REV;
       const long long g0 = REV ? a.n - base - t0 - E : base + t0;
-      if (full && (reinterpret_cast<uintptr_t>(a.y + g0) & 31) == 0) {
+      const long long wlo = REV ? a.n - base - (long long)(w + 1) * 32 * E : base + (long long)w * 32 * E;
+      if (kStaged && full && (reinterpret_cast<uintptr_t>(a.y + wlo) & 15) == 0) {
+        warp_store_staged<T, E, REV>(obuf, x, a.y + wlo, lane);
+      } else if (!kStaged && full && (reinterpret_cast<uintptr_t>(a.y + g0) & 31) == 0) {
         regs_to_global_256<T, E, REV>(a.y + g0, x);
       } else {
 #pragma unroll
@@ -1050,7 +1096,8 @@ template <typename T, bool SEG, bool REV, bool EXCL>
 static cudaError_t launch_scan(const ScanArgs<T>& a, int threads, cudaStream_t s) {
   if (threads == 1024) {
     // persistent: one CTA per SM (cooperative launch), chunks assigned round-robin
-    const size_t smem = ScanGeom<T>::kStageBytes + sizeof(KeepSmem<T>);
+    const size_t smem =
+        ScanGeom<T>::kStageBytes + align_up(sizeof(KeepSmem<T>), 16) + (sizeof(T) == 4 && !REV ? 32 * 2048 : 0);
     auto kern = scan_keep_kernel<T, SEG, REV, EXCL>;
     cudaError_t e = ensure_dyn_smem((const void*)kern, smem);
     if (e != cudaSuccess) return e;
