@@ -35,6 +35,7 @@
 #include "../../include/det_test_hooks.h"
 
 #include <algorithm>
+#include <type_traits>
 
 namespace det {
 namespace {
@@ -747,25 +748,35 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
       const unsigned hwn = lane_heads(hb ^ 1);
       if (next_staged) {
         const T* row = stage + tid * ROW;
+        // FL: the segmented operator; a warp whose lanes hold no head folds
+        // with plain additions (the same values: no flag is ever set)
+        auto fold = [&](auto flagged) {
+          constexpr bool FL = decltype(flagged)::value;
 #pragma unroll
-        for (int q = 0; q < E / PER16; ++q) {
-          const int qq = REV ? E / PER16 - 1 - q : q;
-          const float4 v4 = reinterpret_cast<const float4*>(row)[qq];
-          const T* pv = reinterpret_cast<const T*>(&v4);
+          for (int q = 0; q < E / PER16; ++q) {
+            const int qq = REV ? E / PER16 - 1 - q : q;
+            const float4 v4 = reinterpret_cast<const float4*>(row)[qq];
+            const T* pv = reinterpret_cast<const T*>(&v4);
 #pragma unroll
-          for (int k = 0; k < PER16; ++k) {
-            const int e = q * PER16 + k;
-            const T xe = REV ? pv[PER16 - 1 - k] : pv[k];
-            if (e == 0) {
-              acc = xe;
-              f = hwn & 1u;
-            } else {
-              bool fr;
-              segop<T, SEG>(f, acc, (hwn >> e) & 1u, xe, fr, acc);
-              f = fr;
+            for (int k = 0; k < PER16; ++k) {
+              const int e = q * PER16 + k;
+              const T xe = REV ? pv[PER16 - 1 - k] : pv[k];
+              if (e == 0) {
+                acc = xe;
+                f = FL && (hwn & 1u);
+              } else {
+                bool fr;
+                segop<T, FL>(f, acc, (hwn >> e) & 1u, xe, fr, acc);
+                f = fr;
+              }
             }
           }
-        }
+        };
+        // (f32 only: f64 scans are bound by the FP64 adds, which both paths issue alike)
+        if (SEG && (sizeof(T) == 8 || __any_sync(0xffffffffu, hwn != 0u)))
+          fold(std::integral_constant<bool, SEG>{});
+        else
+          fold(std::integral_constant<bool, false>{});
       } else {
 #pragma unroll
         for (int e = 0; e < E; ++e) {
@@ -795,10 +806,18 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
       segop<T, SEG>(SEG && sm.exclf, sm.excl, SEG && ((sm.wxf[set] >> w) & 1u), sm.wx[set][w], f1, y);
       segop<T, SEG>(f1, y, lxf, lx, f2, y);
       const unsigned hw = lane_heads(hb);
+      if (SEG && (sizeof(T) == 8 || __any_sync(0xffffffffu, hw != 0u))) {
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        y = (SEG && ((hw >> e) & 1u)) ? x[e] : y + x[e];
-        x[e] = y;
+        for (int e = 0; e < E; ++e) {
+          y = ((hw >> e) & 1u) ? x[e] : y + x[e];
+          x[e] = y;
+        }
+      } else {   // no head in the warp's lanes (f32): plain additions
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          y = y + x[e];
+          x[e] = y;
+        }
       }
     }
     if (EXCL && tid == 1023 && c + 1 < a.nchunks) publish<T>(a.tails + c, x[E - 1]);

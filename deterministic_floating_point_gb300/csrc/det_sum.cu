@@ -19,6 +19,8 @@
 //              call's generation number, so nothing is cleared between calls
 //              and a call is one launch.  det_sum_noalloc: the last CTA to
 //              finish, by an integer ticket cleared before the launch.
+#include <cuda.h>
+
 #include <atomic>
 #include <mutex>
 
@@ -279,21 +281,55 @@ static __device__ __align__(256) unsigned char g_sum_noalloc_scratch[kHeaderByte
 namespace {
 constexpr int kMaxDevices = 128;
 std::mutex g_noalloc_mutex;
-void* g_noalloc_scratch[kMaxDevices] = {};
+struct NoallocScratch {
+  void* ptr = nullptr;
+  unsigned long long ctx_id = 0;   // the context the address belongs to (0: not known)
+};
+NoallocScratch g_noalloc_scratch[kMaxDevices];
 
-// Device address of the static array on the current device, looked up once
-// per device.  In host code g_sum_noalloc_scratch names a host-side stand-in,
+// Unique id of the current CUDA context (never reused within the process), or
+// 0 when the driver does not provide one.  A device reset or another context
+// on the same device gets a new id, and with it a new lookup below.
+unsigned long long current_context_id() {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, &id) == CUDA_SUCCESS) return id;
+  return 0;
+}
+
+// Device address of the static array in the current device's current
+// context, looked up on the first call there (and again whenever the context
+// changes).  In host code g_sum_noalloc_scratch names a host-side stand-in,
 // never device memory, so only this address may be handed to a kernel.
 int noalloc_scratch(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DET_ERR_CUDA;
+  const unsigned long long ctx = current_context_id();   // 0 before any context is current: look up again
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_scratch[dev]) {
+  NoallocScratch& e = g_noalloc_scratch[dev];
+  if (!e.ptr || ctx == 0 || e.ctx_id != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_sum_noalloc_scratch) != cudaSuccess || !p) return DET_ERR_CUDA;
-    g_noalloc_scratch[dev] = p;
+    e.ptr = p;
+    e.ctx_id = ctx;
   }
-  *out = g_noalloc_scratch[dev];
+  *out = e.ptr;
   return DET_OK;
 }
 

@@ -108,9 +108,12 @@ int det_sum(const void* x, int64_t n, int dtype, void* out,
  *   out  device, 1 element of dtype (written)
  * Limit: inputs of at most 2^36 bytes (2^34 f32 or 2^33 f64 elements);
  * larger n returns DET_ERR_TOO_LARGE and enqueues nothing.
- * Set-up: the first call on a device (with that device current) looks up
- * the device address of the static array once; make that first call before
- * any stream capture.  The call allocates nothing and frees nothing.
+ * Set-up: the first call in a CUDA context (with its device current) looks
+ * up the device address of the static array in that context, and again
+ * whenever the current context changes -- another context on the device, or
+ * the primary context recreated after cudaDeviceReset (contexts are told
+ * apart by their unique ids); make the first call in a context before any
+ * stream capture.  The call allocates nothing and frees nothing.
  * Sharing: every call on a device uses the same array, which keeps the last
  * call's contents (each call clears the part that must start at zero).
  * Calls whose work can overlap on the GPU -- different streams without

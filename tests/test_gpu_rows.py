@@ -90,8 +90,9 @@ def test_rows_without_prev_and_empty(det, dtype):
 
 def test_rows_workload_full_size_100_runs(det):
     """src 2^20 x 64 f32 N(0,1), rows uniform over a 65,536 x 64 destination:
-    the destination and the previous rows match the oracle, and their SHA-256
-    is the same over repeated runs and block sizes."""
+    at each of the block sizes 128, 256, 1024 and the default, 100 runs; the
+    first one's destination and previous rows hash to the oracle's (SHA-256),
+    and every later run's bits equal the first's (compared on the device)."""
     src, idx, dst0 = workloads.rows_input()
     want_dst, want_prev = oracle.det_scatter_add_rows(dst0, idx, src)
     want = hashlib.sha256(want_dst.tobytes() + want_prev.tobytes()).hexdigest()
@@ -99,10 +100,16 @@ def test_rows_workload_full_size_100_runs(det):
     i = torch.from_numpy(idx).cuda()
     prev = torch.empty_like(s)
     ws = det.workspace(det.lib().det_scatter_add_rows_workspace_bytes(src.shape[0], dst0.shape[0], 64, 0), s.device)
-    for bt, runs in ((128, 5), (256, 5), (1024, 5), (0, 30)):
-        seen = set()
-        for _ in range(runs):
-            dst = torch.from_numpy(dst0.copy()).cuda()
+    dst0_d = torch.from_numpy(dst0).cuda()
+    for bt in (128, 256, 1024, 0):
+        first = None
+        for r in range(100):
+            dst = dst0_d.clone()
             det.det_scatter_add_rows(dst, i, s, prev_out=prev, block_threads=bt, workspace=ws)
-            seen.add(hashlib.sha256(dst.cpu().numpy().tobytes() + prev.cpu().numpy().tobytes()).hexdigest())
-        assert seen == {want}, bt
+            if first is None:
+                got = hashlib.sha256(dst.cpu().numpy().tobytes() + prev.cpu().numpy().tobytes()).hexdigest()
+                assert got == want, bt
+                first = (dst.view(torch.int32).clone(), prev.view(torch.int32).clone())
+            else:
+                assert torch.equal(dst.view(torch.int32), first[0]) and \
+                    torch.equal(prev.view(torch.int32), first[1]), (bt, r)
