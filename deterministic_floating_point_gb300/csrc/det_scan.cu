@@ -35,6 +35,9 @@
 #include "../../include/det_test_hooks.h"
 
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <type_traits>
 
 namespace det {
@@ -301,6 +304,163 @@ __device__ void anchor_chain(const ScanArgs<T>& a) {
       prev = an;
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// Small scans in one thread-block cluster.  When an f64 input has at most
+// kClusterChunks chunks, one cluster holds a CTA per chunk (CTA c = chunk c,
+// 1,024 threads, one virtual lane each).  The chunks' aggregates, and for
+// exclusive scans the chunks' last inclusive values, are exchanged through
+// distributed shared memory across cluster barriers: no descriptor in global
+// memory, nothing to clear, one launch.  The association order is the
+// anchored look-back's: below 32 chunks there is no anchor, and Excl(c) is
+// the tree over lanes L < c holding Agg(c - 1 - L), exactly as above.
+constexpr int kClusterChunks = 16;
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The value at `local` in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ float ld_dsmem(const float* local, unsigned rank) {
+  unsigned r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
+  return v;
+}
+__device__ __forceinline__ double ld_dsmem(const double* local, unsigned rank) {
+  unsigned r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+  double v;
+  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(r) : "memory");
+  return v;
+}
+
+template <typename T, bool REV, bool EXCL>
+__global__ void __launch_bounds__(1024, 1) scan_cluster_kernel(const T* __restrict__ x, T* y, long long n,
+                                                               T* total_out, unsigned int* status) {
+  using G = ScanGeom<T>;
+  constexpr int E = G::E, C = G::C, ROW = G::ROW;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  T* stage = reinterpret_cast<T*>(smem_raw);
+  __shared__ T wt[32], wx[32], last[32];
+  __shared__ T agg_s, tail_s, excl_s;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const long long c = blockIdx.x;   // the grid is one cluster: block index = cluster rank = chunk
+  const long long base = c * C, nvalid = min((long long)C, n - base);
+  auto gidx = [&](long long t) -> long long { return REV ? n - 1 - (base + t) : base + t; };
+  if (c == 0 && tid == 0) *status = DET_OK;   // no wait here can give up: the call's status is ok
+
+  // ---- stage the chunk (scan order): element t -> row t / E, column t % E
+  const bool vec = !REV && nvalid == C && ((reinterpret_cast<uintptr_t>(x + base) & 15) == 0) &&
+                   ((reinterpret_cast<uintptr_t>(y + base) & 15) == 0);
+  constexpr int PER16 = 16 / sizeof(T), NV = C / PER16 / 1024;
+  if (vec) {
+    float4 v[NV];   // every load in flight before the first store
+#pragma unroll
+    for (int k = 0; k < NV; ++k) v[k] = __ldcs(reinterpret_cast<const float4*>(x + base) + tid + k * 1024);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int t = (tid + k * 1024) * PER16;
+      *reinterpret_cast<float4*>(stage + (t / E) * ROW + (t % E)) = v[k];
+    }
+  } else {
+    T v[E];
+#pragma unroll
+    for (int k = 0; k < E; ++k) {
+      const int t = tid + k * 1024;
+      v[k] = t < nvalid ? x[gidx(t)] : absent<T>();
+    }
+#pragma unroll
+    for (int k = 0; k < E; ++k) {
+      const int t = tid + k * 1024;
+      stage[(t / E) * ROW + (t % E)] = v[k];
+    }
+  }
+  __syncthreads();
+
+  // ---- phase 1: lane fold, Kogge-Stone over lanes, then over warps (warp 0)
+  T xr[E];
+  row_to_regs<T, E, false>(stage + tid * ROW, xr);
+  T acc = xr[0];
+#pragma unroll
+  for (int e = 1; e < E; ++e) acc = acc + xr[e];
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const T o = __shfl_up_sync(0xffffffffu, acc, d);
+    if (lane >= d) acc = o + acc;
+  }
+  T lx = __shfl_up_sync(0xffffffffu, acc, 1);
+  if (lane == 0) lx = absent<T>();
+  if (lane == 31) wt[w] = acc;
+  __syncthreads();
+  if (w == 0) {
+    T wa = wt[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const T o = __shfl_up_sync(0xffffffffu, wa, d);
+      if (lane >= d) wa = o + wa;
+    }
+    const T ex = __shfl_up_sync(0xffffffffu, wa, 1);
+    wx[lane] = lane == 0 ? absent<T>() : ex;
+    if (lane == 31) agg_s = wa;   // Agg(c)
+  }
+  cluster_sync_all();   // every chunk's aggregate is visible in the cluster
+
+  // ---- Excl(c): PT over lanes, lane L < c holding Agg(c - 1 - L)
+  if (w == 0) {
+    T v = lane < c ? ld_dsmem(&agg_s, (unsigned)(c - 1 - lane)) : absent<T>();
+    v = warp_pt(v);   // the look-back tree (commutative pairs: the same bits)
+    if (lane == 0) excl_s = v;
+  }
+  __syncthreads();
+
+  // ---- phase 2: element values
+  {
+    T yv = (excl_s + wx[w]) + lx;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      yv = yv + xr[e];
+      xr[e] = yv;
+    }
+  }
+  if (total_out && c == gridDim.x - 1) {
+    const long long tl = nvalid - 1;   // the last element in scan order
+    if (tid == tl / E) {
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if (e == tl % E) *total_out = xr[e];
+    }
+  }
+  if (EXCL) {
+    // previous inclusive value of each lane's first element; the chunk's
+    // first takes the previous chunk's last inclusive value
+    if (lane == 31) last[w] = xr[E - 1];
+    if (tid == 1023) tail_s = xr[E - 1];
+    T pl = __shfl_up_sync(0xffffffffu, xr[E - 1], 1);
+    cluster_sync_all();   // last[] and every chunk's tail visible
+    if (lane == 0) pl = w > 0 ? last[w - 1] : (c > 0 ? ld_dsmem(&tail_s, (unsigned)(c - 1)) : T(0.0));
+#pragma unroll
+    for (int e = E - 1; e > 0; --e) xr[e] = xr[e - 1];
+    xr[0] = pl;
+  }
+  // ---- outputs through the stage rows (each thread rewrites its own row)
+  {
+    T* row = stage + tid * ROW;
+#pragma unroll
+    for (int q = 0; q < E / PER16; ++q) reinterpret_cast<float4*>(row)[q] = reinterpret_cast<const float4*>(xr)[q];
+  }
+  __syncthreads();
+  if (vec) {
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int t = (tid + k * 1024) * PER16;
+      __stcs(reinterpret_cast<float4*>(y + base + t), *reinterpret_cast<const float4*>(stage + (t / E) * ROW + (t % E)));
+    }
+  } else {
+    for (int t = tid; t < nvalid; t += 1024) y[gidx(t)] = stage[(t / E) * ROW + (t % E)];
+  }
+  cluster_sync_all();   // no CTA leaves while another may still read its shared memory
 }
 
 template <typename T, bool SEG, bool REV, bool EXCL>
@@ -1145,6 +1305,59 @@ static cudaError_t launch_scan(const ScanArgs<T>& a, int threads, cudaStream_t s
   return cudaGetLastError();
 }
 
+// Launch the one-cluster scan (a CTA per chunk) when this device can host
+// such a cluster: 1 launched, 0 not possible here, -1 a CUDA error.
+template <typename T>
+static int launch_scan_cluster(const ScanArgs<T>& a, bool rev, bool excl, cudaStream_t s) {
+  void (*k)(const T*, T*, long long, T*, unsigned int*) =
+      rev ? (excl ? scan_cluster_kernel<T, true, true> : scan_cluster_kernel<T, true, false>)
+          : (excl ? scan_cluster_kernel<T, false, true> : scan_cluster_kernel<T, false, false>);
+  const size_t smem = ScanGeom<T>::kStageBytes;
+  const unsigned nc = (unsigned)a.nchunks;
+  // can a cluster of nc such CTAs be resident?  (cached per kernel, device and size)
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, unsigned>, int> fits;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  const auto key = std::make_tuple((const void*)k, dev, nc);
+  int ok = -1;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = fits.find(key);
+    if (it != fits.end()) ok = it->second;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nc);
+  cfg.blockDim = dim3(1024);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = nc;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (ok < 0) {
+    ok = 0;
+    if (ensure_dyn_smem((const void*)k, smem) == cudaSuccess &&
+        (nc <= 8 || cudaFuncSetAttribute((const void*)k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                        cudaSuccess)) {
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, (const void*)k, &cfg) == cudaSuccess && clusters >= 1) ok = 1;
+    }
+    cudaGetLastError();   // a refused query leaves no error behind
+    std::lock_guard<std::mutex> lock(mu);
+    fits[key] = ok;
+  }
+  if (!ok) return 0;
+  launch_begin("det_scan", s);
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, k, a.x, a.y, (long long)a.n, a.total_out, a.status);
+  launch_end(s);
+  return e == cudaSuccess ? 1 : -1;
+}
+
 template <typename T, bool SEG>
 static int scan_impl(const T* x, T* y, long long n, const long long* seg_off, long long nseg, int flags,
                      T* total_out, void* ws, size_t ws_bytes, int bt, cudaStream_t s) {
@@ -1156,9 +1369,16 @@ static int scan_impl(const T* x, T* y, long long n, const long long* seg_off, lo
     if (total_out && cudaMemsetAsync(total_out, 0, sizeof(T), s) != cudaSuccess) return DET_ERR_CUDA;
     return DET_OK;
   }
+  // f64 only: measured faster there (25.8 -> 22.6 us at 164,738 elements, a
+  // chunk's FP64 adds dominate and the memset and look-back go away); for f32
+  // the cluster launch cost more than it saved (14.3 -> 15.7 us)
+  const bool cluster =
+      sizeof(T) == 8 && !SEG && bt == 0 && (n + ScanGeom<T>::C - 1) / ScanGeom<T>::C <= kClusterChunks;
   // one clearing memset: the header, every published word ("unpublished"
   // is all-zero) and, for segmented scans, the head bitmap and chunk flags
-  if (cudaMemsetAsync(w, 0, SEG ? L.total : L.bits, s) != cudaSuccess) return DET_ERR_CUDA;
+  // (the one-cluster path for small inputs publishes nothing in global
+  // memory and writes the status word itself)
+  if (!cluster && cudaMemsetAsync(w, 0, SEG ? L.total : L.bits, s) != cudaSuccess) return DET_ERR_CUDA;
   WsHeader* h = reinterpret_cast<WsHeader*>(ws);
   ScanArgs<T> a;
   a.x = x;
@@ -1195,6 +1415,13 @@ static int scan_impl(const T* x, T* y, long long n, const long long* seg_off, lo
   }
   const int threads = bt ? bt : 1024;
   cudaError_t e;
+  if (cluster) {
+    const int rc = launch_scan_cluster<T>(a, rev, excl, s);
+    if (rc == 1) return DET_OK;     // launched
+    if (rc < 0) return DET_ERR_CUDA;
+    // rc == 0: this device cannot host the cluster: clear, then the general kernels below
+    if (cudaMemsetAsync(w, 0, L.bits, s) != cudaSuccess) return DET_ERR_CUDA;
+  }
   if (rev) {
     e = excl ? launch_scan<T, SEG, true, true>(a, threads, s) : launch_scan<T, SEG, true, false>(a, threads, s);
   } else {

@@ -14,11 +14,12 @@
 //   warp-block 32 lanes = 4 KB, five xor-shuffle levels      -> level 10 / 9
 //   tile       2^tb warp-blocks per CTA (host-chosen power of two), nodes
 //              staged in shared memory and reduced by PT
-//   final      PT over the tile partials, by one CTA.  det_sum: the last
-//              CTA of the grid waits for every tile's flag, tagged with this
-//              call's generation number, so nothing is cleared between calls
-//              and a call is one launch.  det_sum_noalloc: the last CTA to
-//              finish, by an integer ticket cleared before the launch.
+//   final      PT over the tile partials, by one CTA.  det_sum: each tile
+//              publishes its partial in 64-bit words tagged with this call's
+//              generation number; the last CTA of the grid waits for every
+//              tile's words, so nothing is cleared between calls and a call
+//              is one launch.  det_sum_noalloc: the last CTA to finish, by an
+//              integer ticket cleared before the launch.
 #include <cuda.h>
 
 #include <atomic>
@@ -110,17 +111,93 @@ __device__ T cta_pt_global(const T* p, long long L, T* smem_warp) {
   return r;
 }
 
-// FLAGS: tile t publishes flags[t] = gen after its partial; the grid's last
-// CTA waits (bounded in time) for every flag, then forms the final tree and
-// writes the status word itself.  CTAs start in index order, so when the
-// last one runs every other tile has started and only needs to finish; the
-// flags of earlier calls carry other generation numbers, so nothing needs
-// clearing between calls.
+// Tagged partials: a tile's partial sum travels in 64-bit words whose high
+// half is the call's 32-bit generation tag -- one word for f32 (the value in
+// the low half), two for f64 (each carrying 32 bits of the value) -- so that
+// the reader gets tag and value in one load and one round trip.
+template <typename T> struct Tagged;
+template <> struct Tagged<float> {
+  static constexpr int W = 1;
+  __device__ static void put(unsigned long long* p, float v, unsigned tag) {
+    st_release_u64(p, ((unsigned long long)tag << 32) | __float_as_uint(v));
+  }
+  __device__ static bool get(const unsigned long long* p, unsigned tag, float& v) {
+    const unsigned long long w = ld_acquire_u64(p);
+    v = __uint_as_float((unsigned)w);
+    return (unsigned)(w >> 32) == tag;
+  }
+};
+template <> struct Tagged<double> {
+  static constexpr int W = 2;
+  __device__ static void put(unsigned long long* p, double v, unsigned tag) {
+    const unsigned long long b = (unsigned long long)__double_as_longlong(v);
+    st_release_u64(p, ((unsigned long long)tag << 32) | (b & 0xffffffffull));
+    st_release_u64(p + 1, ((unsigned long long)tag << 32) | (b >> 32));
+  }
+  __device__ static bool get(const unsigned long long* p, unsigned tag, double& v) {
+    const unsigned long long lo = ld_acquire_u64(p), hi = ld_acquire_u64(p + 1);
+    v = __longlong_as_double((long long)(((hi & 0xffffffffull) << 32) | (lo & 0xffffffffull)));
+    return (unsigned)(lo >> 32) == tag && (unsigned)(hi >> 32) == tag;
+  }
+};
+
+// PT over the L tagged partials by a whole CTA (the same groups, chunks and
+// trees as cta_pt_global), each partial waited for until it carries `tag`;
+// *ok turns false (in every thread) if a wait gave up.
+template <typename T>
+__device__ T cta_pt_tagged(const unsigned long long* words, long long L, unsigned tag, T* smem_warp, bool* ok) {
+  const int nthreads = blockDim.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
+  long long P = 1;
+  while (P < L) P <<= 1;
+  long long g = P / nthreads;
+  if (g < 1) g = 1;
+  const unsigned long long t0 = globaltimer();
+  bool fine = true;
+  T node;
+  {
+    const long long lo = (long long)tid * g;
+    NodeCounter<T, 6> nc;
+    for (long long c = 0; c < g; c += 8) {
+      T v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const long long idx = lo + c + i;
+        v[i] = absent<T>();
+        if (c + i < g && idx < L) {
+          unsigned polls = 0;
+          while (fine && !Tagged<T>::get(words + Tagged<T>::W * idx, tag, v[i]))
+            if ((++polls & 63u) == 0 && globaltimer() - t0 > kWaitNs) fine = false;
+        }
+      }
+      nc.push(thread_pt(v));
+    }
+    node = nc.result();
+  }
+  *ok = __syncthreads_and(fine);
+  node = warp_pt(node);
+  if (lane == 0) smem_warp[warp] = node;
+  __syncthreads();
+  T r = absent<T>();
+  if (warp == 0) {
+    T v = lane < nwarps ? smem_warp[lane] : absent<T>();
+    r = warp_pt(v);
+  }
+  __syncthreads();
+  return r;
+}
+
+// FLAGS: tile t publishes its partial as tagged words (this call's
+// generation); the grid's last CTA waits (bounded in time) for every tile's
+// words, forms the final tree and writes the status word itself.  CTAs
+// start in index order, so when the last one runs every other tile has
+// started and only needs to finish; words of earlier calls carry other
+// tags, so nothing needs clearing between calls.
 template <typename T, bool VEC, bool FLAGS>
 __global__ void __launch_bounds__(1024)
 sum_kernel(const T* __restrict__ x, long long n, int tb_log2, long long ntiles, T* __restrict__ partials,
-           unsigned int* __restrict__ ticket, T* __restrict__ out, unsigned long long* __restrict__ flags,
-           unsigned long long gen, unsigned int* __restrict__ status) {
+           unsigned int* __restrict__ ticket, T* __restrict__ out, unsigned long long* __restrict__ tagged,
+           unsigned tag, unsigned int* __restrict__ status) {
   using G = SumGeom<T>;
   __shared__ T nodes[1024];
   __shared__ T warp_nodes[32];
@@ -152,11 +229,11 @@ sum_kernel(const T* __restrict__ x, long long n, int tb_log2, long long ntiles, 
     }
     node = warp_pt(node);
     if (lane == 0) {
-      partials[blockIdx.x] = node;
       if (FLAGS) {
-        st_release_u64(flags + blockIdx.x, gen);   // orders the partial before the flag
+        Tagged<T>::put(tagged + Tagged<T>::W * blockIdx.x, node, tag);
         is_last = blockIdx.x == ntiles - 1;
       } else {
+        partials[blockIdx.x] = node;
         __threadfence();
         unsigned int t = atomicAdd(ticket, 1u);
         is_last = (t == (unsigned int)(ntiles - 1));
@@ -166,21 +243,14 @@ sum_kernel(const T* __restrict__ x, long long n, int tb_log2, long long ntiles, 
   __syncthreads();
   if (!is_last) return;
   if (FLAGS) {
-    // every tile's flag carries this call's generation (bounded wait)
+    // the tree over every tile's tagged partial (bounded waits)
     bool ok = true;
-    const unsigned long long t0 = globaltimer();
-    for (long long t = threadIdx.x; t < ntiles && ok; t += blockDim.x) {
-      unsigned polls = 0;
-      while (ld_acquire_u64(flags + t) != gen) {
-        if ((++polls & 63u) == 0 && globaltimer() - t0 > kWaitNs) {
-          ok = false;
-          break;
-        }
-      }
+    const T r = cta_pt_tagged<T>(tagged, ntiles, tag, warp_nodes, &ok);
+    if (threadIdx.x == 0) {
+      if (ok) *out = r;
+      *status = ok ? (unsigned)DET_OK : (unsigned)DET_ERR_LOOKBACK_TIMEOUT;
     }
-    ok = __syncthreads_and(ok);
-    if (threadIdx.x == 0) *status = ok ? (unsigned)DET_OK : (unsigned)DET_ERR_LOOKBACK_TIMEOUT;
-    if (!ok) return;
+    return;
   }
   __threadfence();
   // Partials were written by other CTAs: read them through L2 (volatile).
@@ -214,15 +284,15 @@ static long long sum_ntiles(long long n, int* tb_log2) {
 
 using namespace det;
 
-// Per-call generation numbers of the single-launch path: unique within the
-// process, never 0 (a zeroed flag never matches).
+// Per-call generation numbers of the single-launch path (their low 32 bits,
+// never 0, tag the tiles' partials).
 static std::atomic<unsigned long long> g_sum_gen{0};
 
-// Workspace: header, tile partials, tile flags (one 8-byte word per tile).
+// Workspace: the header, then the tiles' tagged partials (16 bytes a tile).
 extern "C" size_t det_sum_workspace_bytes(int64_t n, int dtype) {
   if (n < 0 || !valid_dtype(dtype)) return 0;
   long long nt = dtype == DET_F32 ? sum_ntiles<float>(n, nullptr) : sum_ntiles<double>(n, nullptr);
-  return kHeaderBytes + align_up((size_t)nt * elem_size(dtype), 256) + align_up((size_t)nt * 8, 256);
+  return kHeaderBytes + align_up((size_t)nt * 16, 256);
 }
 
 template <typename T>
@@ -237,20 +307,19 @@ static int det_sum_impl(const T* x, long long n, T* out, void* ws, size_t ws_byt
     if (cudaMemsetAsync(out, 0, sizeof(T), s) != cudaSuccess) return DET_ERR_CUDA;
     return DET_OK;
   }
-  T* partials = reinterpret_cast<T*>(reinterpret_cast<char*>(ws) + kHeaderBytes);
-  unsigned long long* flags = reinterpret_cast<unsigned long long*>(
-      reinterpret_cast<char*>(ws) + kHeaderBytes + align_up((size_t)nt * sizeof(T), 256));
+  unsigned long long* tagged = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(ws) + kHeaderBytes);
   const int threads = bt ? bt : (tb >= 3 ? 256 : 32 << tb);
   const bool vec = (reinterpret_cast<uintptr_t>(x) % 32) == 0;
   // one launch: the grid's last CTA forms the final tree once every tile's
-  // flag carries this call's generation number
-  const unsigned long long gen = ++g_sum_gen;
+  // partial carries this call's 32-bit generation tag (never 0)
+  unsigned tag = 0;
+  while (tag == 0) tag = (unsigned)++g_sum_gen;
   launch_begin("det_sum", s);
   if (vec)
-    sum_kernel<T, true, true><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out, flags, gen,
+    sum_kernel<T, true, true><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, nullptr, &h->ticket, out, tagged, tag,
                                                                 &h->status);
   else
-    sum_kernel<T, false, true><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out, flags, gen,
+    sum_kernel<T, false, true><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, nullptr, &h->ticket, out, tagged, tag,
                                                                  &h->status);
   launch_end(s);
   return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
@@ -351,10 +420,10 @@ int det_sum_noalloc_impl(const T* x, long long n, T* out, int bt, cudaStream_t s
   launch_begin("det_sum_noalloc", s);
   if (vec)
     sum_kernel<T, true, false><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out, nullptr,
-                                                                 0ull, nullptr);
+                                                                 0u, nullptr);
   else
     sum_kernel<T, false, false><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out, nullptr,
-                                                                  0ull, nullptr);
+                                                                  0u, nullptr);
   launch_end(s);
   return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
 }
