@@ -1074,7 +1074,7 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
 // coalesced warp accesses (any alignment) and reach their lanes from padded
 // rows.
 template <typename T, bool REV, bool EXCL>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(128, 6)   // at most 64 (f32) / 72 (f64) registers: 6+ CTAs per SM
 restart_kernel(const T* x, T* y, long long n, const long long* __restrict__ off, long long S,
                unsigned int* __restrict__ status) {
   using G = ScanGeom<T>;
