@@ -965,6 +965,10 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
     // at a time: the FP64 add rate bounds them, and this keeps the add pipe
     // busy while stores and shared-memory reads are in flight (one barrier
     // fewer per chunk).  Same values: only the instruction order changes.
+    // The interleaved form is for f64 only: f32 scans, bound by HBM rather
+    // than by their additions, measured slower with it (e.g. 477 -> 567 us
+    // forward exclusive at 2^28).
+    constexpr bool kMergedPath = sizeof(T) == 8;
     // (the forward inclusive full scan written out on its own: measured 11 %
     // faster than the general form below, which is faster for the others)
     if constexpr (sizeof(T) == 8 && !SEG && !REV && !EXCL) {
@@ -1028,8 +1032,9 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
       if (next_staged) prefetch(cn, hb ^ 1, 0);
       continue;
     }
-    if constexpr (sizeof(T) == 8) {
+    if constexpr (kMergedPath) {
       constexpr int P = 32 / (int)sizeof(T);   // elements per 32-byte group
+      constexpr int Q = 16 / (int)sizeof(T);   // elements per 16-byte chunk of a stage row
       bool f1, f2;
       T y;
       segop<T, SEG>(SEG && sm.exclf, sm.excl, SEG && ((sm.wxf[set] >> w) & 1u), sm.wx[set][w], f1, y);
@@ -1043,19 +1048,18 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
       const long long want = a.n - 1 - base - t0;   // the last element of the scan, if in this lane
       const bool has_total = a.total_out && want >= 0 && want < E;
       T tv = absent<T>();
-      // outputs o0..o3 of group q (scan order) to memory
-      auto store_group = [&](int q, T o0, T o1, T o2, T o3) {
+      // outputs o[] of group q (scan order) to memory
+      auto store_group = [&](int q, const T (&o)[P]) {
         if (vstore) {
-          if (REV)   // group q lands at the mirrored group, its elements reversed
-            asm volatile("st.global.v4.f64 [%0], {%1,%2,%3,%4};" ::"l"(a.y + g0 + (E / P - 1 - q) * P), "d"(o3),
-                         "d"(o2), "d"(o1), "d"(o0)
-                         : "memory");
-          else
-            asm volatile("st.global.v4.f64 [%0], {%1,%2,%3,%4};" ::"l"(a.y + g0 + q * P), "d"(o0), "d"(o1),
-                         "d"(o2), "d"(o3)
-                         : "memory");
+          if (REV) {   // group q lands at the mirrored group, its elements reversed
+            T r[P];
+#pragma unroll
+            for (int k = 0; k < P; ++k) r[k] = o[P - 1 - k];
+            st_256(a.y + g0 + (E / P - 1 - q) * P, r);
+          } else {
+            st_256(a.y + g0 + q * P, o);
+          }
         } else {
-          const T o[P] = {o0, o1, o2, o3};
 #pragma unroll
           for (int k = 0; k < P; ++k)
             if (t0 + q * P + k < nvalid) a.y[gidx(c, t0 + q * P + k)] = o[k];
@@ -1065,15 +1069,16 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
       auto promote_group = [&](int q) {
         if (!promote) return;
 #pragma unroll
-        for (int h = 0; h < P / 2; ++h) {
+        for (int h = 0; h < P / Q; ++h) {
+          T v[Q];
           if (REV) {   // scan element e of the row sits at row index E - 1 - e
-            const double2 v2 = reinterpret_cast<const double2*>(row)[(E - q * P - P) / 2 + h];
-            x[q * P + P - 1 - 2 * h] = v2.x;
-            x[q * P + P - 2 - 2 * h] = v2.y;
+            *reinterpret_cast<float4*>(v) = reinterpret_cast<const float4*>(row)[(E - q * P - P) / Q + h];
+#pragma unroll
+            for (int k = 0; k < Q; ++k) x[q * P + P - 1 - (h * Q + k)] = v[k];
           } else {
-            const double2 v2 = reinterpret_cast<const double2*>(row)[q * (P / 2) + h];
-            x[q * P + 2 * h] = v2.x;
-            x[q * P + 2 * h + 1] = v2.y;
+            *reinterpret_cast<float4*>(v) = reinterpret_cast<const float4*>(row)[q * (P / Q) + h];
+#pragma unroll
+            for (int k = 0; k < Q; ++k) x[q * P + h * Q + k] = v[k];
           }
         }
       };
@@ -1096,19 +1101,11 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
             x[e] = y;
             if (e == want) tv = y;
           }
-          if (vstore) {
-            if (REV)
-              asm volatile("st.global.v4.f64 [%0], {%1,%2,%3,%4};" ::"l"(a.y + g0 + (E / P - 1 - q) * P),
-                           "d"(x[q * P + 3]), "d"(x[q * P + 2]), "d"(x[q * P + 1]), "d"(x[q * P])
-                           : "memory");
-            else
-              asm volatile("st.global.v4.f64 [%0], {%1,%2,%3,%4};" ::"l"(a.y + g0 + q * P), "d"(x[q * P]),
-                           "d"(x[q * P + 1]), "d"(x[q * P + 2]), "d"(x[q * P + 3])
-                           : "memory");
-          } else {
+          {
+            T o[P];
 #pragma unroll
-            for (int k = 0; k < P; ++k)
-              if (t0 + q * P + k < nvalid) a.y[gidx(c, t0 + q * P + k)] = x[q * P + k];
+            for (int k = 0; k < P; ++k) o[k] = x[q * P + k];
+            store_group(q, o);
           }
           promote_group(q);
         }
@@ -1122,8 +1119,11 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
         for (int q = 0; q < E / P; ++q) {
           incl_group(q);
           if (q > 0) {
-            store_group(q, ex(q * P, prev_last), ex(q * P + 1, x[q * P]), ex(q * P + 2, x[q * P + 1]),
-                        ex(q * P + 3, x[q * P + 2]));
+            T o[P];
+            o[0] = ex(q * P, prev_last);
+#pragma unroll
+            for (int k = 1; k < P; ++k) o[k] = ex(q * P + k, x[q * P + k - 1]);
+            store_group(q, o);
           }
           prev_last = x[q * P + P - 1];
           if (q > 0) promote_group(q);
@@ -1133,7 +1133,13 @@ __global__ void __launch_bounds__(1024, 1) scan_keep_kernel(ScanArgs<T> a) {
         T pl = __shfl_up_sync(0xffffffffu, prev_last, 1);
         __syncthreads();
         if (lane == 0) pl = (w > 0) ? sm.last[w - 1] : T(0.0);   // chunk start: written later
-        store_group(0, ex(0, pl), ex(1, x[0]), ex(2, x[1]), ex(3, x[2]));
+        {
+          T o[P];
+          o[0] = ex(0, pl);
+#pragma unroll
+          for (int k = 1; k < P; ++k) o[k] = ex(k, x[k - 1]);
+          store_group(0, o);
+        }
         promote_group(0);
         if (tid == 0) {
           // the chunk's first element is the previous chunk's last inclusive
