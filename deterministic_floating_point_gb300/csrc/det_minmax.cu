@@ -79,18 +79,23 @@ __device__ __forceinline__ unsigned long long group_reduce(unsigned g, unsigned 
   return ((unsigned long long)rh << 32) | rl;
 }
 
-// One record per lane: the lanes sharing lane 0's bin combine their keys and
-// lane 0 applies one atomic (a hot bin costs one atomic per warp instead of
-// 32); the other lanes apply their own.
+// One record per lane: when other lanes share lane 0's bin, those lanes
+// combine their keys first and one of them applies a single atomic (a hot bin
+// costs one atomic per warp instead of 32); otherwise -- the common case --
+// every lane applies its own in one warp-wide atomic instruction.
 template <typename T, bool MAX>
-__device__ __forceinline__ void apply(typename KeyOf<T>::U* keys, long long b, bool valid, typename KeyOf<T>::U k) {
+__device__ __forceinline__ void apply(typename KeyOf<T>::U* keys, int b, bool valid, typename KeyOf<T>::U k) {
   const int lane = threadIdx.x & 31;
-  const long long b0 = __shfl_sync(0xffffffffu, b, 0);
+  const int b0 = __shfl_sync(0xffffffffu, b, 0);
   const bool in0 = valid && b == b0;
   const unsigned g = __ballot_sync(0xffffffffu, in0);
-  if (in0) {
-    const auto r = group_reduce<MAX>(g, k);
-    if (lane == __ffs(g) - 1) key_atomic<MAX>(keys + b, r);
+  if (g & (g - 1)) {   // two or more lanes in lane 0's bin (warp-uniform)
+    if (in0) {
+      const auto r = group_reduce<MAX>(g, k);
+      if (lane == __ffs(g) - 1) key_atomic<MAX>(keys + b, r);
+    } else if (valid) {
+      key_atomic<MAX>(keys + b, k);
+    }
   } else if (valid) {
     key_atomic<MAX>(keys + b, k);
   }
@@ -152,8 +157,8 @@ minmax_scatter_kernel(const int32_t* __restrict__ bins, const T* __restrict__ va
     }
 #pragma unroll
     for (int e = 0; e < kPerLane; ++e) {
-      const long long b = bb[e];
-      const bool valid = b >= 0 && b < m;
+      const int b = bb[e];
+      const bool valid = b >= 0 && (long long)b < m;
       apply<T, MAX>(keys, valid ? b : -1, valid, to_key<T, MAX>(vv[e]));
     }
   }
