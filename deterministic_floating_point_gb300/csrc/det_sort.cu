@@ -624,12 +624,17 @@ template <int kBoundsPer>
 __global__ void sort_bounds_kernel(const int32_t* __restrict__ keys, const unsigned int* __restrict__ n_valid,
                                    long long m, int32_t* __restrict__ seg, long long n) {
   dep_wait();   // launched early (programmatic dependent launch): wait for the previous kernel
-  const long long i0 = kBoundsPer * ((long long)blockIdx.x * blockDim.x + threadIdx.x);
-  const long long N = min((long long)*n_valid, n);
-  if (i0 > N) return;
-  auto clampk = [&](int32_t k) { return max(-1LL, min((long long)k, m)); };
+  // sort sizes, positions and keys are below 2^31: 32-bit arithmetic throughout
+  // (64-bit compares and clamps made this kernel bound by its integer pipe)
+  // (positions as unsigned: i0 + e stays below 2^32 for every sort size)
+  const int m32 = (int)m;
+  const long long i0l = (long long)kBoundsPer * ((long long)blockIdx.x * blockDim.x + threadIdx.x);
+  const unsigned N = (unsigned)min((long long)*n_valid, n);
+  if (i0l > (long long)N) return;
+  const unsigned i0 = (unsigned)i0l;
+  auto clampk = [&](int32_t k) { return max(-1, min(k, m32)); };
   int32_t kr[kBoundsPer];   // the keys at i0 + e (m from N on)
-  const long long before = i0 == 0 ? -1 : clampk(__ldg(keys + i0 - 1));
+  const int before = i0 == 0 ? -1 : clampk(__ldg(keys + i0 - 1));
   if (i0 + kBoundsPer <= N && (reinterpret_cast<uintptr_t>(keys + i0) & 15) == 0) {
 #pragma unroll
     for (int q = 0; q < kBoundsPer / 4; ++q) {
@@ -643,12 +648,12 @@ __global__ void sort_bounds_kernel(const int32_t* __restrict__ keys, const unsig
 #pragma unroll
     for (int e = 0; e < kBoundsPer; ++e) kr[e] = i0 + e < N ? __ldg(keys + i0 + e) : 0;
   }
-  long long prev = before;
+  int prev = before;
 #pragma unroll
   for (int e = 0; e < kBoundsPer; ++e) {
     if (i0 + e > N) break;
-    const long long cur = i0 + e < N ? clampk(kr[e]) : m;
-    for (long long b = prev + 1; b <= cur; ++b) seg[b] = (int32_t)(i0 + e);
+    const int cur = i0 + e < N ? clampk(kr[e]) : m32;
+    for (int b = prev + 1; b <= cur; ++b) seg[b] = (int32_t)(i0 + e);
     prev = cur;
   }
 }
