@@ -706,7 +706,7 @@ constexpr int kMediumGroup = 1024;   // groups up to this size are reduced by on
 // (negated for NEG) padded with absent terms, then the in-register tree --
 // PT padded to W, which is PT of the group.
 template <typename T, bool NEG, int W>
-__device__ __forceinline__ T thread_group_pt(const T* __restrict__ p, long long len) {
+__device__ __forceinline__ T thread_group_pt(const T* __restrict__ p, int len) {
   T v[W];
 #pragma unroll
   for (int e = 0; e < W; ++e) {
@@ -756,7 +756,7 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
   if (wmax > 0) {
     T t = absent<T>();
     const T* g = vals + lo;
-    const long long gl = in_chunk ? len : 0;
+    const int gl = in_chunk ? (int)len : 0;
     if (wmax <= 1)
       t = thread_group_pt<T, NEG, 1>(g, gl);
     else if (wmax <= 2)
@@ -777,7 +777,9 @@ segtree_bins_kernel(const T* __restrict__ vals, const int32_t* __restrict__ seg,
     // counter.  Neighbouring bins have similar sizes in practice, so the
     // lanes of a warp mostly run the same number of chunks.
     NodeCounter<T, 6> nc;
-    for (long long c = 0; c < len; c += CW) nc.push(thread_group_pt<T, NEG, CW>(vals + lo + c, len - c));
+    const T* g = vals + lo;
+    const int l32 = (int)len;   // at most kMediumGroup: 32-bit loop arithmetic
+    for (int c = 0; c < l32; c += CW) nc.push(thread_group_pt<T, NEG, CW>(g + c, l32 - c));
     out[b * ostride] = out[b * ostride] + nc.result();
   }
   // long groups: their blocks are reserved (the reservation order does not
