@@ -121,8 +121,9 @@ template <> struct Tagged<float> {
   __device__ static void put(unsigned long long* p, float v, unsigned tag) {
     st_release_u64(p, ((unsigned long long)tag << 32) | __float_as_uint(v));
   }
+  // the value travels in the tagged word itself: a relaxed load suffices
   __device__ static bool get(const unsigned long long* p, unsigned tag, float& v) {
-    const unsigned long long w = ld_acquire_u64(p);
+    const unsigned long long w = ld_relaxed_u64(p);
     v = __uint_as_float((unsigned)w);
     return (unsigned)(w >> 32) == tag;
   }
@@ -134,8 +135,10 @@ template <> struct Tagged<double> {
     st_release_u64(p, ((unsigned long long)tag << 32) | (b & 0xffffffffull));
     st_release_u64(p + 1, ((unsigned long long)tag << 32) | (b >> 32));
   }
+  // one 16-byte relaxed load; each half is checked against the tag on its own
   __device__ static bool get(const unsigned long long* p, unsigned tag, double& v) {
-    const unsigned long long lo = ld_acquire_u64(p), hi = ld_acquire_u64(p + 1);
+    unsigned long long lo, hi;
+    ld_relaxed_v2u64(p, lo, hi);
     v = __longlong_as_double((long long)(((hi & 0xffffffffull) << 32) | (lo & 0xffffffffull)));
     return (unsigned)(lo >> 32) == tag && (unsigned)(hi >> 32) == tag;
   }
@@ -160,14 +163,21 @@ __device__ T cta_pt_tagged(const unsigned long long* words, long long L, unsigne
     NodeCounter<T, 6> nc;
     for (long long c = 0; c < g; c += 8) {
       T v[8];
+      bool got[8];
+      // first look at all eight words (loads in flight together), then wait
+      // only for those not yet tagged with this call
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const long long idx = lo + c + i;
         v[i] = absent<T>();
-        if (c + i < g && idx < L) {
-          unsigned polls = 0;
-          while (fine && !Tagged<T>::get(words + Tagged<T>::W * idx, tag, v[i]))
-            if ((++polls & 63u) == 0 && globaltimer() - t0 > kWaitNs) fine = false;
+        got[i] = !(c + i < g && idx < L) || Tagged<T>::get(words + Tagged<T>::W * idx, tag, v[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        unsigned polls = 0;
+        while (!got[i] && fine) {
+          got[i] = Tagged<T>::get(words + Tagged<T>::W * (lo + c + i), tag, v[i]);
+          if ((++polls & 63u) == 0 && globaltimer() - t0 > kWaitNs) fine = false;
         }
       }
       nc.push(thread_pt(v));

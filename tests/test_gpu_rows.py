@@ -113,3 +113,35 @@ def test_rows_workload_full_size_100_runs(det):
             else:
                 assert torch.equal(dst.view(torch.int32), first[0]) and \
                     torch.equal(prev.view(torch.int32), first[1]), (bt, r)
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("W", [2, 4, 8, 100, 128])
+@pytest.mark.parametrize("src_off,dst_off", [(0, 0), (2, 0), (0, 1)])
+@pytest.mark.parametrize("ordered", [False, True])
+def test_rows_layouts(det, dtype, W, src_off, dst_off, ordered):
+    """Row lengths and base offsets that select each access form: pair
+    accesses (even W, every array on a pair boundary) and single columns (an
+    odd element offset of dst), each with one long group and many short
+    ones."""
+    rng = np.random.default_rng(W * 7 + src_off * 3 + dst_off)
+    M, R = 30_001, 900
+    src = rng.standard_normal((M, W)).astype(dtype)
+    idx = rng.integers(-2, R + 2, M, dtype=np.int32)
+    idx[:2500] = 11                                        # one long group: many rounds
+    dst0 = rng.standard_normal((R, W)).astype(dtype)
+    f = oracle.det_scatter_add_rows_ordered if ordered else oracle.det_scatter_add_rows
+    want_dst, want_prev = f(dst0, idx, src)
+    sbuf = torch.zeros(src_off + M * W, dtype=torch.float32 if dtype == np.float32 else torch.float64, device="cuda")
+    dbuf = torch.zeros(dst_off + R * W, dtype=sbuf.dtype, device="cuda")
+    s = sbuf[src_off:].view(M, W)
+    s.copy_(torch.from_numpy(src))
+    dst = dbuf[dst_off:].view(R, W)
+    dst.copy_(torch.from_numpy(dst0))
+    prev = torch.full_like(s, 99.0)
+    ws = det.workspace(det.lib().det_scatter_add_rows_workspace_bytes(M, R, W, 0 if dtype == np.float32 else 1),
+                       s.device)
+    det.det_scatter_add_rows(dst, torch.from_numpy(idx).cuda(), s, prev_out=prev, workspace=ws, ordered=ordered)
+    assert det.read_status(ws) == 0
+    assert dst.cpu().numpy().tobytes() == want_dst.tobytes()
+    assert prev.cpu().numpy().tobytes() == want_prev.tobytes()
