@@ -153,3 +153,13 @@ def test_skewed_workload_full_size(det, dtype):
     assert out.tobytes() == want_out.tobytes()
     assert np.array_equal(seg, want_seg)
     assert np.array_equal(perm, want_perm)
+
+
+@pytest.mark.parametrize("n,m", [((1 << 25) + 1357, 1024), ((1 << 25) + 1357, 1 << 20), ((1 << 26) + 999, 1024)])
+def test_many_tiles(det, n, m):
+    """Sorts of many tiles: with 4,096-record tiles (block_threads 128),
+    2^25 + 1,357 records make 8,193 tiles and 2^26 + 999 records 16,385, so
+    the column scan reads each tile group in several batches and the last
+    tile is ragged; one- and two-pass keys."""
+    values, bins, out0 = workloads.scatter_input(n=n, num_bins=m, dtype=np.float32, seed=n % 89)
+    check(det, out0, bins, values, bts=(128,))
