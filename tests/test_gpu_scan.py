@@ -84,15 +84,16 @@ def test_scan_block_sizes_and_in_place(det, dtype, bt):
 
 @pytest.mark.parametrize("dtype", [np.float32, np.float64])
 def test_scan_small_workload_100_runs(det, dtype):
-    """The 164,738-element lognormal input: 100 runs at three block sizes give
-    the oracle's SHA-256 for every flag combination."""
+    """The 164,738-element lognormal input: 100 runs at three block sizes and
+    the default launch (for f64 the one-cluster path) give the oracle's
+    SHA-256 for every flag combination."""
     x_np = workloads.scan_input(dtype=dtype)
     x = torch.from_numpy(x_np).cuda()
     y = torch.empty_like(x)
     ws = det.workspace(det.lib().det_scan_workspace_bytes(x.numel(), 0 if dtype == np.float32 else 1), x.device)
     for flags in FLAGS:
         want = hashlib.sha256(oracle.det_scan(x_np, flags)[0].tobytes()).hexdigest()
-        for bt in (128, 256, 1024):
+        for bt in (0, 128, 256, 1024):
             seen = set()
             for _ in range(100):
                 det.det_scan(x, y, flags=flags, block_threads=bt, workspace=ws)

@@ -71,12 +71,13 @@ def test_sum_signed_zero_and_fingerprint(det, dtype):
 @pytest.mark.parametrize("dtype,bound", [(np.float32, 2e-6), (np.float64, 1e-14)])
 def test_sum_workload_100_runs_three_block_sizes(det, dtype, bound):
     """The 2^20-element uniform[0,12) workload: SHA-256 of the result bits is
-    the oracle's over 100 runs at block sizes 128, 256 and 1024."""
+    the oracle's over 100 runs at block sizes 128, 256 and 1024 and at the
+    default launch."""
     x = workloads.sum_input(dtype=dtype)
     want = hashlib.sha256(bits(oracle.det_sum(x), dtype)).hexdigest()
     t = torch.from_numpy(x).cuda()
     out = torch.empty(1, dtype=t.dtype, device="cuda")
-    for bt in (128, 256, 1024):
+    for bt in (0, 128, 256, 1024):
         hashes = set()
         for _ in range(100):
             det.det_sum(t, out, block_threads=bt)
@@ -88,8 +89,9 @@ def test_sum_workload_100_runs_three_block_sizes(det, dtype, bound):
 
 @pytest.mark.parametrize("dtype", [np.float32, np.float64])
 def test_sum_full_size_supplement(det, dtype):
-    """n = 2^28, the size the kernel's roofline is measured on."""
+    """n = 2^28, the size the kernel's roofline is measured on, at the default
+    launch the bench times and two block sizes."""
     x = workloads.sum_input(n=1 << 28, dtype=dtype, seed=0)
     want = bits(oracle.det_sum(x), dtype)
-    for bt in (128, 1024):
+    for bt in (0, 128, 1024):
         assert bits(gpu_sum(det, x, bt), dtype) == want
