@@ -40,6 +40,22 @@ BLOCK_THREADS = 0      # --block-threads: launch shape of the library calls (nev
 N_OVERRIDE = 0         # --n: element count of the sum and scan workloads (smaller cases for profiler captures)
 
 
+def max_over_ranks(torch, value, device, world):
+    """The largest of the ranks' values, on every rank (a job takes as long as
+    its slowest rank).  One rank: the value itself."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, elems, steps, total_ms):
+    """Gelem/s of the whole job: each of the `world` ranks processes `elems`
+    elements per step, `steps` steps in `total_ms` (the slowest rank's time)."""
+    return world * elems * steps / (total_ms * 1e-3) / 1e9
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -790,13 +806,9 @@ def run_det(args, torch, rank, world):
         torch.cuda.synchronize()
     launches = det.launch_count() - launches0
     ktimes, kernels = time_steps(torch, wl, args.steps, flush, det.KernelTimer)
-    total_ms = sum(times)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(torch, sum(times), dev, world)
     ms_per_step = total_ms / args.steps
-    value = world * wl["elems"] * args.steps / (total_ms * 1e-3) / 1e9
+    value = whole_job_rate(world, wl["elems"], args.steps, total_ms)
     step_bytes = wl["step_bytes"]
 
     # dominant kernel: average launch duration over the timed steps
@@ -826,9 +838,12 @@ def run_det(args, torch, rank, world):
                          "algo_adds_per_launch": adds, "hbm": hbm})
 
     # end to end through host buffers (pinned), same metric
+    # (whole job: every rank's steps, timed from a common barrier, the slowest rank's time)
     for _ in range(2):
         wl["e2e_step"]()
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -836,9 +851,9 @@ def run_det(args, torch, rank, world):
         wl["e2e_step"]()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    e2e = {"value": wl["elems"] / (e2e_ms * 1e-3) / 1e9, "unit": "Gelem/s",
-           "h2d_bytes_per_step": wl["h2d"], "d2h_bytes_per_step": wl["d2h"], "ms_per_step": e2e_ms}
+    e2e_total = max_over_ranks(torch, e0.elapsed_time(e1), dev, world)
+    e2e = {"value": whole_job_rate(world, wl["elems"], args.steps, e2e_total), "unit": "Gelem/s",
+           "h2d_bytes_per_step": wl["h2d"], "d2h_bytes_per_step": wl["d2h"], "ms_per_step": e2e_total / args.steps}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
