@@ -9,20 +9,23 @@
 // those nodes, so neither the block size nor the grid enters the bits.
 //
 // Layout of the work:
-//   lane       128 contiguous bytes (32 f32 / 16 f64) = 4 x 256-bit loads,
-//              reduced in registers by PT                 -> level 5 / 4 node
-//   warp-block 32 lanes = 4 KB, five xor-shuffle levels      -> level 10 / 9
+//   lane       32 contiguous f32 (128 bytes) or 64 f64 (four 128-byte
+//              chunks) by 256-bit loads, reduced in registers by PT
+//                                                          -> level 5 / 6 node
+//   warp-block 32 lanes = 4 KB / 16 KB, five xor-shuffle levels -> level 10 / 11
 //   tile       2^tb warp-blocks per CTA (host-chosen power of two), nodes
 //              staged in shared memory and reduced by PT
 //   final      PT over the tile partials, by one CTA.  det_sum: each tile
-//              publishes its partial in 64-bit words tagged with this call's
-//              generation number; the last CTA of the grid waits for every
-//              tile's words, so nothing is cleared between calls and a call
-//              is one launch.  det_sum_noalloc: the last CTA to finish, by an
-//              integer ticket cleared before the launch.
+//              publishes its partial in words tagged with this call's 64-bit
+//              tag; the last CTA of the grid waits for every tile's words, so
+//              nothing is cleared between calls and a call is one launch.
+//              det_sum_noalloc: the last CTA to finish, by an integer ticket
+//              cleared before the launch.
 #include <cuda.h>
 
 #include <atomic>
+#include <chrono>
+#include <random>
 #include <mutex>
 
 #include "det_common.cuh"
@@ -111,36 +114,39 @@ __device__ T cta_pt_global(const T* p, long long L, T* smem_warp) {
   return r;
 }
 
-// Tagged partials: a tile's partial sum travels in 64-bit words whose high
-// half is the call's 32-bit generation tag -- one word for f32 (the value in
-// the low half), two for f64 (each carrying 32 bits of the value) -- so that
-// the reader gets tag and value in one load and one round trip.
-template <typename T> struct Tagged;
-template <> struct Tagged<float> {
-  static constexpr int W = 1;
-  __device__ static void put(unsigned long long* p, float v, unsigned tag) {
-    st_release_u64(p, ((unsigned long long)tag << 32) | __float_as_uint(v));
-  }
-  // the value travels in the tagged word itself: a relaxed load suffices
-  __device__ static bool get(const unsigned long long* p, unsigned tag, float& v) {
-    const unsigned long long w = ld_relaxed_u64(p);
-    v = __uint_as_float((unsigned)w);
-    return (unsigned)(w >> 32) == tag;
-  }
-};
-template <> struct Tagged<double> {
+// Tagged partials: a tile's partial sum travels in two 64-bit words, read by
+// one 16-byte load.  Their high halves hold the two halves of the call's
+// 64-bit tag; their low halves hold the value's bits (f64: low then high 32
+// bits; f32: the value in both).  The workspace may hold anything from
+// earlier use -- other calls' words, or any other data -- so a tile counts
+// as published only when both halves carry this call's tag.  Tags are
+// distinct for every call of the process (a bijective mix of a call counter
+// and a per-process seed), with neither half zero: earlier calls' words
+// never match, and other contents match a given tag by chance only (2^-64
+// per word for data that is not itself such a word).
+template <typename T> struct Tagged {
   static constexpr int W = 2;
-  __device__ static void put(unsigned long long* p, double v, unsigned tag) {
-    const unsigned long long b = (unsigned long long)__double_as_longlong(v);
-    st_release_u64(p, ((unsigned long long)tag << 32) | (b & 0xffffffffull));
-    st_release_u64(p + 1, ((unsigned long long)tag << 32) | (b >> 32));
-  }
-  // one 16-byte relaxed load; each half is checked against the tag on its own
-  __device__ static bool get(const unsigned long long* p, unsigned tag, double& v) {
+  __device__ static void put(unsigned long long* p, T v, unsigned long long tag) {
     unsigned long long lo, hi;
-    ld_relaxed_v2u64(p, lo, hi);
-    v = __longlong_as_double((long long)(((hi & 0xffffffffull) << 32) | (lo & 0xffffffffull)));
-    return (unsigned)(lo >> 32) == tag && (unsigned)(hi >> 32) == tag;
+    if (sizeof(T) == 8) {
+      const unsigned long long b = (unsigned long long)__double_as_longlong((double)v);
+      lo = b & 0xffffffffull;
+      hi = b >> 32;
+    } else {
+      lo = hi = __float_as_uint((float)v);
+    }
+    st_release_u64(p, (tag & 0xffffffff00000000ull) | lo);
+    st_release_u64(p + 1, (tag << 32) | hi);
+  }
+  // the value travels in the tagged words themselves: relaxed loads suffice
+  __device__ static bool get(const unsigned long long* p, unsigned long long tag, T& v) {
+    unsigned long long w0, w1;
+    ld_relaxed_v2u64(p, w0, w1);
+    if (sizeof(T) == 8)
+      v = (T)__longlong_as_double((long long)(((w1 & 0xffffffffull) << 32) | (w0 & 0xffffffffull)));
+    else
+      v = (T)__uint_as_float((unsigned)w0);
+    return (w0 >> 32) == (tag >> 32) && (w1 >> 32) == (tag & 0xffffffffull);
   }
 };
 
@@ -148,7 +154,8 @@ template <> struct Tagged<double> {
 // trees as cta_pt_global), each partial waited for until it carries `tag`;
 // *ok turns false (in every thread) if a wait gave up.
 template <typename T>
-__device__ T cta_pt_tagged(const unsigned long long* words, long long L, unsigned tag, T* smem_warp, bool* ok) {
+__device__ T cta_pt_tagged(const unsigned long long* words, long long L, unsigned long long tag, T* smem_warp,
+                           bool* ok) {
   const int nthreads = blockDim.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
   long long P = 1;
@@ -297,9 +304,41 @@ static long long sum_ntiles(long long n, int* tb_log2) {
 
 using namespace det;
 
-// Per-call generation numbers of the single-launch path (their low 32 bits,
-// never 0, tag the tiles' partials).
+// Per-call tags of the single-launch path: the splitmix64 finalizer (Steele,
+// Lea and Flood, "Fast splittable pseudorandom number generators", 2014; a
+// bijection of 64-bit words) of a call counter XOR a per-process seed, so no
+// two calls of the process share a tag; tags with a zero half are skipped.
 static std::atomic<unsigned long long> g_sum_gen{0};
+
+static unsigned long long mix64(unsigned long long z) {
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+  return z ^ (z >> 31);
+}
+
+static unsigned long long process_seed() {
+  static const unsigned long long seed = [] {
+    unsigned long long v = 0;
+    try {
+      std::random_device rd;
+      v = ((unsigned long long)rd() << 32) ^ rd();
+    } catch (...) {
+    }
+    // mixed with the clock and an address of this process as well
+    v ^= (unsigned long long)std::chrono::high_resolution_clock::now().time_since_epoch().count();
+    v ^= (unsigned long long)reinterpret_cast<uintptr_t>(&g_sum_gen) << 7;
+    return v;
+  }();
+  return seed;
+}
+
+static unsigned long long next_sum_tag() {
+  const unsigned long long seed = process_seed();
+  for (;;) {
+    const unsigned long long t = mix64(++g_sum_gen ^ seed);
+    if ((t >> 32) != 0 && (t & 0xffffffffull) != 0) return t;
+  }
+}
 
 // Workspace: the header, then the tiles' tagged partials (16 bytes a tile).
 extern "C" size_t det_sum_workspace_bytes(int64_t n, int dtype) {
@@ -324,9 +363,8 @@ static int det_sum_impl(const T* x, long long n, T* out, void* ws, size_t ws_byt
   const int threads = bt ? bt : (tb >= 3 ? 256 : 32 << tb);
   const bool vec = (reinterpret_cast<uintptr_t>(x) % 32) == 0;
   // one launch: the grid's last CTA forms the final tree once every tile's
-  // partial carries this call's 32-bit generation tag (never 0)
-  unsigned tag = 0;
-  while (tag == 0) tag = (unsigned)++g_sum_gen;
+  // partial carries this call's tag
+  const unsigned long long tag = next_sum_tag();
   launch_begin("det_sum", s);
   if (vec)
     sum_kernel<T, true, true><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, nullptr, &h->ticket, out, tagged, tag,

@@ -95,3 +95,33 @@ def test_sum_full_size_supplement(det, dtype):
     want = bits(oracle.det_sum(x), dtype)
     for bt in (0, 128, 1024):
         assert bits(gpu_sum(det, x, bt), dtype) == want
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("n", [1 << 20, (1 << 24) + 5])
+def test_sum_workspace_with_leftover_contents(det, dtype, n):
+    """The workspace is never cleared: a call must find its tiles' partials
+    among whatever the buffer held before -- small integers in every 32-bit
+    half (int32 data), all-ones bytes, random bytes, and the partials of
+    earlier calls on other data.  Each call equals the oracle."""
+    x = workloads.sum_input(n=n, dtype=dtype, seed=11)
+    want = bits(oracle.det_sum(x), dtype)
+    other = torch.from_numpy(workloads.sum_input(n=n, dtype=dtype, seed=12)).cuda()
+    t = torch.from_numpy(x).cuda()
+    out = torch.empty(1, dtype=t.dtype, device="cuda")
+    code = 0 if dtype == np.float32 else 1
+    ws = det.workspace(det.lib().det_sum_workspace_bytes(n, code), t.device)
+    words = ws[: (ws.numel() // 8) * 8].view(torch.int32)
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    fills = [
+        lambda: words.copy_(torch.arange(1, words.numel() + 1, dtype=torch.int32, device="cuda") % 4096),
+        lambda: ws.fill_(0xFF),
+        lambda: ws.copy_(torch.randint(0, 256, (ws.numel(),), dtype=torch.uint8, device="cuda", generator=gen)),
+        lambda: det.det_sum(other, workspace=ws),
+    ]
+    for fill in fills:
+        for _ in range(25):
+            fill()
+            det.det_sum(t, out, workspace=ws)
+            assert bits(out.cpu().numpy()[0], dtype) == want
+            assert det.read_status(ws) == 0
