@@ -362,6 +362,28 @@ static int det_sum_impl(const T* x, long long n, T* out, void* ws, size_t ws_byt
   unsigned long long* tagged = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(ws) + kHeaderBytes);
   const int threads = bt ? bt : (tb >= 3 ? 256 : 32 << tb);
   const bool vec = (reinterpret_cast<uintptr_t>(x) % 32) == 0;
+  // Under stream capture the tag would be fixed into the graph and shared by
+  // every replay, and a replay could take an earlier replay's partials for
+  // its own: there the call is a clearing memset of the header (captured
+  // too, so it runs on every replay) and the ticket form of the kernel.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+    cudaGetLastError();   // not a launch failure: take the form that is safe either way
+    cap = cudaStreamCaptureStatusActive;
+  }
+  if (cap != cudaStreamCaptureStatusNone) {
+    if (cudaMemsetAsync(h, 0, kHeaderBytes, s) != cudaSuccess) return DET_ERR_CUDA;
+    T* partials = reinterpret_cast<T*>(tagged);
+    launch_begin("det_sum", s);
+    if (vec)
+      sum_kernel<T, true, false><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out, nullptr,
+                                                                   0ull, &h->status);
+    else
+      sum_kernel<T, false, false><<<(unsigned)nt, threads, 0, s>>>(x, n, tb, nt, partials, &h->ticket, out, nullptr,
+                                                                    0ull, &h->status);
+    launch_end(s);
+    return cudaGetLastError() == cudaSuccess ? DET_OK : DET_ERR_CUDA;
+  }
   // one launch: the grid's last CTA forms the final tree once every tile's
   // partial carries this call's tag
   const unsigned long long tag = next_sum_tag();

@@ -81,6 +81,11 @@ extern "C" {
  * and grid size cannot change it.  n = 0 gives +0.0.
  *   x   device, n elements of dtype, contiguous, any alignment
  *   out device, 1 element of dtype (written)
+ * Enqueued work: one launch, which clears nothing (the workspace may hold
+ * anything; each call tags its tile partials with a tag of its own).  On a
+ * stream under capture the call enqueues a clearing memset of the
+ * workspace header and a launch instead, so every replay of the graph
+ * starts clean; the bits are the same either way.
  * Follows: Day 68 "Floating point and reproducibility", sections "Contracts
  * from tolerance to fixed bits" (items 1-2) and "Fix the order of every
  * addition" (the atomic tail replaced by a fixed tree).

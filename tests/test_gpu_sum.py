@@ -125,3 +125,33 @@ def test_sum_workspace_with_leftover_contents(det, dtype, n):
             det.det_sum(t, out, workspace=ws)
             assert bits(out.cpu().numpy()[0], dtype) == want
             assert det.read_status(ws) == 0
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("n", [1 << 20, (1 << 24) + 5])
+def test_sum_captured_in_a_cuda_graph(det, dtype, n):
+    """det_sum captured once in a CUDA graph and replayed over changing inputs
+    in the same buffer: every replay equals the oracle on its own input (no
+    replay may take another replay's tile partials)."""
+    xs = [workloads.sum_input(n=n, dtype=dtype, seed=s) for s in (21, 22, 23)]
+    wants = [bits(oracle.det_sum(x), dtype) for x in xs]
+    hosts = [torch.from_numpy(x) for x in xs]
+    t = torch.empty(n, dtype=DT[dtype], device="cuda")
+    out = torch.empty(1, dtype=t.dtype, device="cuda")
+    code = 0 if dtype == np.float32 else 1
+    ws = det.workspace(det.lib().det_sum_workspace_bytes(n, code), t.device)
+    t.copy_(hosts[0])
+    det.det_sum(t, out, workspace=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        det.det_sum(t, out, workspace=ws)
+    for r in range(30):
+        k = r % 3
+        t.copy_(hosts[k])
+        g.replay()
+        assert bits(out.cpu().numpy()[0], dtype) == wants[k], r
+    # the same workspace outside the graph afterwards
+    t.copy_(hosts[1])
+    det.det_sum(t, out, workspace=ws)
+    assert bits(out.cpu().numpy()[0], dtype) == wants[1]
