@@ -16,14 +16,18 @@
  *   keeps no pointer after a call returns and allocates nothing.
  * - `workspace` is caller-owned device memory of at least the size the
  *   matching *_workspace_bytes() query returns, 256-byte aligned.  Its
- *   contents on entry do not matter; the call zeroes what it needs with
- *   cudaMemsetAsync on `stream`.  Its first bytes hold the device status word
- *   read by det_read_status().  One workspace must not be shared by calls
- *   that may run at the same time.
+ *   contents on entry do not matter: the call zeroes what it needs with
+ *   cudaMemsetAsync on `stream`, or (det_sum) tells its own words apart by a
+ *   per-call tag.  Its first bytes hold the device status word read by
+ *   det_read_status().  One workspace must not be shared by calls that may
+ *   run at the same time.
  * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *   stream).  Work is only enqueued: no call synchronizes, allocates or copies
  *   to the host, so every call that takes a workspace can be captured in a
- *   CUDA graph.
+ *   CUDA graph.  A captured call can be replayed: the state it leaves in the
+ *   workspace is cleared by its own captured memsets on the next replay, and
+ *   det_sum, which otherwise clears nothing, takes a clearing form on a
+ *   capturing stream (its per-call tag would be frozen into the graph).
  * - `block_threads` selects the CUDA block size: 0 (the default) or one of
  *   128, 256, 512, 1024.  It changes the launch shape only, never the bits.
  *   The sorts behind the scatter calls sort tiles of 4,096 records (CTAs of
