@@ -204,12 +204,14 @@ __device__ T cta_pt_tagged(const unsigned long long* words, long long L, unsigne
   return r;
 }
 
-// FLAGS: tile t publishes its partial as tagged words (this call's
-// generation); the grid's last CTA waits (bounded in time) for every tile's
-// words, forms the final tree and writes the status word itself.  CTAs
-// start in index order, so when the last one runs every other tile has
-// started and only needs to finish; words of earlier calls carry other
-// tags, so nothing needs clearing between calls.
+// FLAGS: tile t publishes its partial as words tagged with this call's tag;
+// the grid's last CTA waits (bounded in time) for every tile's words, forms
+// the final tree and writes the status word itself.  CTAs start in index
+// order, so when the last one runs every other tile has started and only
+// needs to finish; words of earlier calls carry other tags, so nothing
+// needs clearing between calls.  Otherwise (the ticket form): each tile
+// stores its partial, and the CTA that takes the last ticket of a counter
+// cleared before the launch forms the final tree.
 template <typename T, bool VEC, bool FLAGS>
 __global__ void __launch_bounds__(1024)
 sum_kernel(const T* __restrict__ x, long long n, int tb_log2, long long ntiles, T* __restrict__ partials,
