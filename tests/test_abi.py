@@ -89,3 +89,34 @@ def test_scan_withhold_hook_checks_its_limit(lib):
     assert lib.det_test_scan_withhold(5, 0) == 1                 # no limit
     assert lib.det_test_scan_withhold(5, 3 * 10**9) == 1         # above the 2 s default
     assert lib.det_test_scan_withhold(-1, 0) == 0                # clearing always works
+
+
+def test_no_cpu_path_when_the_library_is_missing(tmp_path):
+    """With libdet.so absent every call raises: nothing falls back to CPU code."""
+    import subprocess
+    import sys
+    code = (
+        "import sys; sys.path.insert(0, %r)\n"
+        "import torch\n"
+        "from deterministic_floating_point_gb300 import det\n"
+        "det.LIB_PATH = %r\n"
+        "det._lib = None\n"
+        "try:\n"
+        "    det.lib()\n"
+        "except RuntimeError as e:\n"
+        "    print('raised', 'missing' in str(e))\n"
+    ) % (ROOT, str(tmp_path / "absent" / "libdet.so"))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == "raised True"
+
+
+def test_host_tensors_are_refused(lib):
+    """The binding takes device tensors only; host tensors raise before any call."""
+    import torch
+    from deterministic_floating_point_gb300 import det
+    x = torch.ones(16)
+    for call in (lambda: det.det_sum(x), lambda: det.det_scan(x),
+                 lambda: det.det_scatter_add(torch.zeros(4), torch.zeros(16, dtype=torch.int32), x)):
+        with pytest.raises(ValueError):
+            call()
