@@ -61,22 +61,6 @@ __device__ __forceinline__ void ld_nc_256(const double* p, double (&v)[4]) {
                : "l"(p));
 }
 
-// Plain (coherent) 256-bit load, for data another block of this grid may have
-// written earlier in the same launch.
-__device__ __forceinline__ void ld_256(const float* p, float (&v)[8]) {
-  asm volatile("ld.global.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
-                 "=f"(v[6]), "=f"(v[7])
-               : "l"(p)
-               : "memory");
-}
-__device__ __forceinline__ void ld_256(const double* p, double (&v)[4]) {
-  asm volatile("ld.global.v4.f64 {%0,%1,%2,%3}, [%4];"
-               : "=d"(v[0]), "=d"(v[1]), "=d"(v[2]), "=d"(v[3])
-               : "l"(p)
-               : "memory");
-}
-
 __device__ __forceinline__ void st_256(float* p, const float (&v)[8]) {
   asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(v[0]),
                "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
@@ -163,37 +147,15 @@ struct NodeCounter {
 };
 
 // ---------------------------------------------------------------------------
-// Memory-model helpers for flags and published values.
-__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
-  unsigned int v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_u32(unsigned int* p, unsigned int v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
+// Memory-model helpers for published values.
 __device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-// Relaxed loads of words that carry their own payload (nothing else is read
-// on their strength), so several can be in flight at once.
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
+// A relaxed 16-byte load of words that carry their own payload (nothing else
+// is read on their strength), so several can be in flight at once.
 __device__ __forceinline__ void ld_relaxed_v2u64(const unsigned long long* p, unsigned long long& a,
                                                  unsigned long long& b) {
   asm volatile("ld.relaxed.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
-}
-__device__ __forceinline__ void ld_acquire_v2u64(const unsigned long long* p, unsigned long long& a,
-                                                 unsigned long long& b) {
-  asm volatile("ld.acquire.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 
 // Record a device-detected error in the status word (first error wins).
